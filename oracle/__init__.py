@@ -1,0 +1,121 @@
+"""CPU fp64 attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library in
+``tiled_attention_bwd_gb300``) never imports, links or calls it, and the two
+share no code.
+
+Functions take numpy arrays (any float dtype; bf16 torch tensors should be
+converted with ``.double().numpy()``, which is exact) of shape [B, H, N, d]
+or [BH, N, d], and return float64 arrays of the same shape (LSE: [..., N]).
+
+What each function follows:
+  fwd         -- the definition O = softmax(scale Q K^T [+ causal mask]) V and
+                 LSE = ln sum_j exp(scale q_i . k_j), two-pass per row
+                 ("RTX Flash Attention Implementation COMPLETE", "Usage
+                 Examples": forward(q, k, v, causal, scale) -> output, lse).
+  fwd_online  -- the same result by the running-max / running-sum update of
+                 "RTX Flash Attention Implementation COMPLETE", "Online
+                 Softmax Algorithm", over key tiles, optionally lazy.
+  bwd         -- gradients dQ, dK, dV of L with dL/dO = dout, P recomputed
+                 from the row's LSE ("GPU Performance Optimization Batch 1 --
+                 Design Spec", Item 3, backward paragraph).  The formulas come
+                 from the chain rule; the pages do not print them.
+
+Every function is pinned by tests/test_oracle.py against things other than
+itself: torch fp64 autograd, central finite differences, closed forms and
+invariants (see that file).
+"""
+import ctypes
+
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build_oracle()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.oracle_fwd.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_int,
+                                   ctypes.c_double, dp, dp]
+        lib.oracle_fwd.restype = None
+        lib.oracle_fwd_online.argtypes = [dp, dp, dp, i64, i64, i64,
+                                          ctypes.c_int, ctypes.c_double, i64,
+                                          ctypes.c_double, dp, dp]
+        lib.oracle_fwd_online.restype = None
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64,
+                                   ctypes.c_int, ctypes.c_double, dp, dp, dp]
+        lib.oracle_bwd.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _as_f64(x):
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shape(q):
+    if q.ndim == 4:
+        B, H, N, d = q.shape
+        return B * H, N, d
+    if q.ndim == 3:
+        return q.shape
+    raise ValueError("expected [B,H,N,d] or [BH,N,d], got %s" % (q.shape,))
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs with (OMP_NUM_THREADS, else all cores)."""
+    return int(_load().oracle_num_threads())
+
+
+def fwd(q, k, v, causal: bool, scale: float):
+    """Two-pass fp64 forward; returns (O, LSE)."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    BH, N, d = _shape(q)
+    o = np.empty_like(q)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, d, int(bool(causal)),
+                       float(scale), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def fwd_online(q, k, v, causal: bool, scale: float, tile: int = 1,
+               tau: float = 0.0):
+    """Online-softmax fp64 forward over key tiles of `tile` keys; with
+    tau > 0 the reference max is kept until exceeded by more than tau."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    BH, N, d = _shape(q)
+    o = np.empty_like(q)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    _load().oracle_fwd_online(_ptr(q), _ptr(k), _ptr(v), BH, N, d,
+                              int(bool(causal)), float(scale), int(tile),
+                              float(tau), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def bwd(q, k, v, dout, causal: bool, scale: float):
+    """fp64 backward; returns (dQ, dK, dV).  O and D come from the oracle's
+    own fp64 forward of the same inputs."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    BH, N, d = _shape(q)
+    dq = np.empty_like(q)
+    dk = np.empty_like(q)
+    dv = np.empty_like(q)
+    _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), BH, N, d,
+                       int(bool(causal)), float(scale), _ptr(dq), _ptr(dk),
+                       _ptr(dv))
+    return dq, dk, dv

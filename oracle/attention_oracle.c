@@ -1,0 +1,233 @@
+/*
+ * attention_oracle.c -- CPU fp64 oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
+ * its Python binding) links, imports or calls this file.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark use it.  It shares
+ * no code, header, table or helper with the CUDA path.
+ *
+ * What it computes is the plain definition of the operation described on
+ *   "RTX Flash Attention Implementation COMPLETE", section "Usage Examples"
+ *   (forward(q, k, v, causal, scale) -> output, lse over tensors laid out as
+ *   [batch, heads, seq_len, head_dim]; backward(dout, q, k, v, output, lse,
+ *   causal, scale) -> dq, dk, dv),
+ * i.e. O = softmax(scale * Q K^T [+ causal mask]) V, its per-row log-sum-exp,
+ * and the gradients of a loss L with dL/dO = dout.
+ *
+ * All arithmetic is in double precision, no blocking or fusion beyond the
+ * definition: one row of scores at a time (so an N x N matrix is never held),
+ * two passes over that row (max, then sum of exponentials).  Every (b,h) head
+ * is independent; heads are spread over OpenMP threads.
+ *
+ * Readings of points the pages leave open (each listed in the design notes):
+ *   - LSE is the natural logarithm of sum_j exp(scale * q_i . k_j).
+ *   - Causal means key j is visible to query i iff j <= i (equal lengths).
+ *   - scale multiplies Q K^T before the mask and the softmax.
+ *
+ * The gradient formulas are not printed on the pages; they follow from the
+ * definition by the chain rule through softmax:
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = dO_i . O_i,
+ *   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ * The pages' backward recomputes P from the saved LSE ("GPU Performance
+ * Optimization Batch 1 -- Design Spec", Item 3, the FlashAttention-3 backward
+ * paragraph; "RTX Flash Attention Implementation COMPLETE", "Flash Attention
+ * Backward Kernel: Gradient Recomputation").  Here P is recomputed from the
+ * oracle's own fp64 LSE in the same way.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static double dot(const double* a, const double* b, int64_t d) {
+  double s = 0.0;
+  for (int64_t t = 0; t < d; ++t) s += a[t] * b[t];
+  return s;
+}
+
+/* Number of keys visible to query row i. */
+static int64_t visible_keys(int64_t i, int64_t n, int causal) {
+  return causal ? (i + 1) : n;
+}
+
+/*
+ * Scores s_j = scale * q_i . k_j for the visible keys, then the two-pass
+ * log-sum-exp: m = max_j s_j, Z = sum_j exp(s_j - m), lse = m + ln Z.
+ * Returns lse; s[] holds the scores.
+ */
+static double row_scores_lse(const double* qi, const double* k, int64_t nvis,
+                             int64_t d, double scale, double* s) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < nvis; ++j) {
+    s[j] = scale * dot(qi, k + j * d, d);
+    if (s[j] > m) m = s[j];
+  }
+  double z = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) z += exp(s[j] - m);
+  return m + log(z);
+}
+
+/*
+ * Forward.  q, k, v, o: [BH, N, d] row-major doubles; lse: [BH, N].
+ * P_ij = exp(s_ij - lse_i); O_i = sum_j P_ij v_j.
+ */
+void oracle_fwd(const double* q, const double* k, const double* v,
+                int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                double* o, double* lse) {
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+      const double* qh = q + bh * N * d;
+      const double* kh = k + bh * N * d;
+      const double* vh = v + bh * N * d;
+      double* oh = o + bh * N * d;
+      for (int64_t i = 0; i < N; ++i) {
+        int64_t nvis = visible_keys(i, N, causal);
+        double l = row_scores_lse(qh + i * d, kh, nvis, d, scale, s);
+        lse[bh * N + i] = l;
+        double* oi = oh + i * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+          double p = exp(s[j] - l);
+          const double* vj = vh + j * d;
+          for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
+        }
+      }
+    }
+    free(s);
+  }
+}
+
+/*
+ * Forward by the online softmax of "RTX Flash Attention Implementation
+ * COMPLETE", section "Online Softmax Algorithm": a running max m and a running
+ * sum l are updated as new scores arrive, m' = max(m, x),
+ * l' = l * exp(m - m') + exp(x - m').  The output accumulator is rescaled by the
+ * same factor exp(m - m').  Scores arrive in tiles of `tile` keys; with
+ * tile = 1 this is the page's element-by-element rule.
+ *
+ * `tau` >= 0 enables the lazy variant: the reference maximum is only replaced
+ * when the tile maximum exceeds it by more than tau (natural-log units);
+ * otherwise exp(x - m) may exceed 1 but the result is unchanged.
+ * tau = 0 is the eager rule.
+ */
+void oracle_fwd_online(const double* q, const double* k, const double* v,
+                       int64_t BH, int64_t N, int64_t d, int causal,
+                       double scale, int64_t tile, double tau, double* o,
+                       double* lse) {
+  if (tile < 1) tile = 1;
+#pragma omp parallel
+  {
+    double* acc = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(tile));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+      const double* qh = q + bh * N * d;
+      const double* kh = k + bh * N * d;
+      const double* vh = v + bh * N * d;
+      for (int64_t i = 0; i < N; ++i) {
+        int64_t nvis = visible_keys(i, N, causal);
+        double m = -INFINITY, l = 0.0;
+        for (int64_t t = 0; t < d; ++t) acc[t] = 0.0;
+        for (int64_t j0 = 0; j0 < nvis; j0 += tile) {
+          int64_t j1 = j0 + tile < nvis ? j0 + tile : nvis;
+          double mt = -INFINITY;
+          for (int64_t j = j0; j < j1; ++j) {
+            s[j - j0] = scale * dot(qh + i * d, kh + j * d, d);
+            if (s[j - j0] > mt) mt = s[j - j0];
+          }
+          double mnew = m;
+          if (m == -INFINITY || mt > m + tau) mnew = (mt > m ? mt : m);
+          double alpha = (m == -INFINITY) ? 0.0 : exp(m - mnew);
+          l *= alpha;
+          for (int64_t t = 0; t < d; ++t) acc[t] *= alpha;
+          for (int64_t j = j0; j < j1; ++j) {
+            double p = exp(s[j - j0] - mnew);
+            l += p;
+            const double* vj = vh + j * d;
+            for (int64_t t = 0; t < d; ++t) acc[t] += p * vj[t];
+          }
+          m = mnew;
+        }
+        double* oi = o + (bh * N + i) * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] = acc[t] / l;
+        lse[bh * N + i] = m + log(l);
+      }
+    }
+    free(s);
+    free(acc);
+  }
+}
+
+/*
+ * Backward.  q, k, v, dout: [BH, N, d]; outputs dq, dk, dv: [BH, N, d].
+ * Per query row i: recompute the scores and lse_i, P_ij = exp(s_ij - lse_i),
+ * O_i = sum_j P_ij v_j, D_i = dO_i . O_i; then for each visible key j:
+ *   dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i += scale dS_ij k_j,  dK_j += scale dS_ij q_i,  dV_j += P_ij dO_i.
+ */
+void oracle_bwd(const double* q, const double* k, const double* v,
+                const double* dout, int64_t BH, int64_t N, int64_t d,
+                int causal, double scale, double* dq, double* dk, double* dv) {
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double* oi = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+      const double* qh = q + bh * N * d;
+      const double* kh = k + bh * N * d;
+      const double* vh = v + bh * N * d;
+      const double* doh = dout + bh * N * d;
+      double* dqh = dq + bh * N * d;
+      double* dkh = dk + bh * N * d;
+      double* dvh = dv + bh * N * d;
+      memset(dqh, 0, sizeof(double) * (size_t)(N * d));
+      memset(dkh, 0, sizeof(double) * (size_t)(N * d));
+      memset(dvh, 0, sizeof(double) * (size_t)(N * d));
+      for (int64_t i = 0; i < N; ++i) {
+        int64_t nvis = visible_keys(i, N, causal);
+        const double* qi = qh + i * d;
+        const double* doi = doh + i * d;
+        double l = row_scores_lse(qi, kh, nvis, d, scale, s);
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+          s[j] = exp(s[j] - l); /* s now holds P_ij */
+          const double* vj = vh + j * d;
+          for (int64_t t = 0; t < d; ++t) oi[t] += s[j] * vj[t];
+        }
+        double D = dot(doi, oi, d);
+        double* dqi = dqh + i * d;
+        for (int64_t j = 0; j < nvis; ++j) {
+          double p = s[j];
+          const double* kj = kh + j * d;
+          const double* vj = vh + j * d;
+          double dp = dot(doi, vj, d);
+          double ds = p * (dp - D);
+          double* dkj = dkh + j * d;
+          double* dvj = dvh + j * d;
+          for (int64_t t = 0; t < d; ++t) {
+            dqi[t] += scale * ds * kj[t];
+            dkj[t] += scale * ds * qi[t];
+            dvj[t] += p * doi[t];
+          }
+        }
+      }
+    }
+    free(oi);
+    free(s);
+  }
+}
