@@ -1,0 +1,377 @@
+"""Benchmark: attention forward + backward TFLOP/s on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+
+One step = fa_fwd + fa_bwd over the whole workload (default: 4x64x4096x128
+causal, the headline shape), inputs resident in HBM.  Each rank runs the full
+workload on its own GPU (weak scaling, no collective on the data path); the
+reported value is the total algorithmic FLOPs of all ranks divided by the
+slowest rank's time.  Rank 0 prints one JSON line.
+
+FLOP convention: forward = 4 B H N^2 d (halved when causal), backward = 2.5 x
+forward, step = 3.5 x forward.
+
+--impl reference times the CPU fp64 oracle (the plain definition, no tuning)
+on the host cores, each step a bounded sample of the same workload (the last
+128 query rows of one head per core, forward + backward), in the same unit.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd and fwd+bwd TFLOP/s (bf16) and % of GB300 dense "
+          "BF16 peak")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return (float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained",
+                                                       p["bf16_tflops"])),
+                float(p["hbm_gbs"]), "measured")
+    except (OSError, KeyError, ValueError):
+        return (FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (identity for a single process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2],
+                "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample(w, heads, rows):
+    """Run the CPU oracle (forward + backward) on the last `rows` query rows
+    of `heads` heads of workload `w`.  Returns (algorithmic FLOPs, seconds)."""
+    import numpy as np
+    import oracle
+    from tiled_attention_bwd_gb300.workloads import make_inputs
+    inp = make_inputs(1, heads, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    q, k, v, do = (inp[n].double().numpy()[0] for n in ("q", "k", "v", "do"))
+    r0 = w.N - rows
+    t0 = time.perf_counter()
+    oracle.fwd_rows(q, k, v, w.causal, w.scale, r0, w.N)
+    oracle.bwd_rows(q, k, v, do, w.causal, w.scale, r0, w.N)
+    dt = time.perf_counter() - t0
+    if w.causal:
+        pairs = float(np.sum(np.arange(r0, w.N) + 1))
+    else:
+        pairs = float(rows) * w.N
+    flops = heads * pairs * 4.0 * w.d * 3.5
+    return flops, dt
+
+
+def run_reference(args, w, rank, world):
+    """CPU oracle arm: rank 0 only; other ranks exit without work."""
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.num_threads()
+    rows = 128
+    for _ in range(args.warmup):
+        oracle_sample(w, cores, rows)
+    total_flops, total_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(w, cores, rows)
+        total_flops += f
+        total_s += s
+    value = total_flops / total_s / 1e12
+    sample = ("last %d query rows of %d heads (one per core) of %s, fwd+bwd, "
+              "per step" % (rows, cores, w.name))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                   "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local):
+    import torch
+    from tiled_attention_bwd_gb300 import (fa_bwd, fa_bwd_set_phase_events,
+                                           fa_bwd_workspace_size,
+                                           fa_check_device_status, fa_fwd,
+                                           load_library)
+    from tiled_attention_bwd_gb300.workloads import workload_inputs
+
+    load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak_burst, peak_sust, hbm_peak, peak_src = load_peaks()
+
+    inp_cpu = workload_inputs(w)
+    q, k, v, do = (inp_cpu[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa_bwd_workspace_size(w.B, w.H, w.N, w.d),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+        fa_bwd(q, k, v, o, lse, do, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+               workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    if fa_check_device_status(dev) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    # -------- timed region: whole step, plus the backward main kernel alone
+    K = args.steps
+    main_ev = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        fa_bwd_set_phase_events(*main_ev[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    fa_bwd_set_phase_events(None, None)
+    clocks = sampler.stop() if sampler else None
+    if fa_check_device_status(dev) != 0:
+        raise RuntimeError("device status error in the timed region")
+    step_ms_local = t_start.elapsed_time(t_end) / K
+    main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / K
+    step_ms = max_over_ranks(step_ms_local, world, dev)
+
+    # -------- forward alone (same inputs), for the forward-only figure
+    fw_s = torch.cuda.Event(enable_timing=True)
+    fw_e = torch.cuda.Event(enable_timing=True)
+    for _ in range(max(1, args.warmup)):
+        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    fw_s.record(stream)
+    for _ in range(K):
+        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+    fw_e.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = max_over_ranks(fw_s.elapsed_time(fw_e) / K, world, dev)
+
+    # -------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {n: torch.empty_like(host["q"]).pin_memory()
+                for n in ("o", "dq", "dk", "dv")}
+        lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+                t.copy_(host[n], non_blocking=True)
+            step()
+            for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+                outs[n].copy_(t, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        s, e = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        K_e2e = max(3, K // 4)
+        s.record(stream)
+        for _ in range(K_e2e):
+            e2e_step()
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(s.elapsed_time(e) / K_e2e, world, dev)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+        d2h = (sum(outs[n].numel() * outs[n].element_size() for n in outs)
+               + lse_h.numel() * 4)
+        e2e = {"value": world * (w.fwd_flops() + w.bwd_flops()) / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    step_flops = w.fwd_flops() + w.bwd_flops()
+    value = world * step_flops / (step_ms * 1e-3) / 1e12
+    fwd_tflops = world * w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+    main_tflops = w.bwd_flops() / (main_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.num_threads()
+        rows = 512
+        f, s_ = oracle_sample(w, cores, rows)
+        cpu = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores,
+               "kind": "oracle",
+               "sample": "last %d query rows of %d heads of %s, fwd+bwd, "
+                         "%.1f s" % (rows, cores, w.name, s_)}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                   "d": w.d, "causal": w.causal, "scale": w.scale,
+                   "qk_mult": w.qk_mult, "per_gpu": "full workload per rank",
+                   "l2": "inputs larger than L2 (%d MB per tensor)" % (
+                       q.numel() * 2 // 2**20)},
+        "fwd": {"value": fwd_tflops, "unit": "TFLOP/s", "ms": fwd_ms,
+                "frac_of_peak": fwd_tflops / world / peak_burst},
+        "fwd_bwd_frac_of_peak": value / world / peak_burst,
+        "peak": {"bf16_tflops": peak_burst, "bf16_tflops_sustained": peak_sust,
+                 "source": peak_src},
+        "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor",
+                     "achieved": main_tflops, "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": main_tflops / peak_burst,
+                     "peak_source": "%s bf16 burst" % peak_src,
+                     "ms_per_launch": main_ms, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    from tiled_attention_bwd_gb300.workloads import HEADLINE, WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        raise SystemExit("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

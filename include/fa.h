@@ -1,0 +1,147 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) tiled attention library, libfa.so.
+ *
+ * The library computes exact scaled-dot-product attention and its training
+ * backward pass, tile by tile with an online softmax, so that the N x N score
+ * matrix never reaches device memory:
+ *
+ *   forward(q, k, v, causal, scale) -> output, lse
+ *   backward(dout, q, k, v, output, lse, causal, scale) -> dq, dk, dv
+ *
+ * which is the interface of "RTX Flash Attention Implementation COMPLETE",
+ * section "Usage Examples" (basic forward pass; training with backward pass),
+ * with tensors laid out as [batch, heads, seq_len, head_dim].  The operation
+ * itself is O = softmax(scale * Q K^T [+ causal mask]) V with the online
+ * softmax of the same page's "Online Softmax Algorithm" section (running max
+ * m, running sum l); the backward recomputes P from the saved LSE, as in
+ * "GPU Performance Optimization Batch 1 -- Design Spec", Item 3
+ * ("FlashAttention-3 Blackwell"), backward paragraph.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors q, k, v, o, dout, dq, dk, dv are contiguous row-major bfloat16
+ *    arrays of shape [B, H, N, d] in device memory (element (b,h,i,t) at
+ *    ((b*H + h)*N + i)*d + t).  Their base addresses must be 16-byte aligned.
+ *  - lse is a contiguous float32 array [B, H, N] in device memory holding the
+ *    natural-log log-sum-exp of each row's scaled scores:
+ *    lse[b,h,i] = ln sum_j exp(scale * q_i . k_j) over the visible keys j.
+ *    4-byte alignment is enough.
+ *  - causal = 1 lets query i see keys j <= i (equal query and key lengths);
+ *    causal = 0 lets every query see every key.
+ *  - scale multiplies Q K^T before the mask and the softmax; it must be finite
+ *    and > 0 (usually 1/sqrt(d)).
+ *  - Supported: d in {64, 128}; N >= 1 of any size (tiles past N are masked);
+ *    B, H >= 1.  B, H or N equal to 0 is an empty problem: the call returns
+ *    FA_OK and touches nothing (pointers may then be NULL).
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every compute entry point is asynchronous on that stream:
+ *    FA_OK means the kernels were launched.  A failure detected on the device
+ *    (a pipeline wait that ran past its time limit) is reported later by
+ *    fa_check_device_status().
+ *  - Memory: all tensors and the workspace belong to the caller.  The library
+ *    allocates no device memory per call; it keeps one small device status
+ *    record per GPU for the lifetime of the process.
+ *  - Errors: invalid arguments are rejected on the host before anything is
+ *    launched (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED); a failing CUDA call
+ *    returns FA_ERR_CUDA.  No entry point aborts the process.
+ *  - The device must be an sm_103a (GB300-class) GPU; kernels are compiled
+ *    for that target only.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size or scale */
+  FA_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. d = 96)    */
+  FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed          */
+  FA_ERR_DEVICE_TIMEOUT = 4,  /* a kernel's bounded pipeline wait expired   */
+  FA_ERR_WORKSPACE = 5        /* workspace missing or smaller than needed   */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v : in,  bf16 [B,H,N,d]
+ *   o       : out, bf16 [B,H,N,d]   o_i = sum_j softmax_j(scale q_i.k_j) v_j
+ *   lse     : out, fp32 [B,H,N]     natural-log log-sum-exp per row
+ * o and lse may not alias the inputs.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
+                 float* lse, int B, int H, int N, int d, int causal,
+                 float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
+ * accumulator [B,H,N,d] followed by two fp32 per-row vectors
+ * (D_i = dO_i . O_i and LSE_i * log2(e)) padded to whole 128-row tiles.
+ * Returns 0 for an empty problem or unsupported d.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass.
+ *   q, k, v   : in,  bf16 [B,H,N,d]  the forward's inputs
+ *   o, lse    : in,  bf16 [B,H,N,d] / fp32 [B,H,N]  the forward's outputs
+ *   dout      : in,  bf16 [B,H,N,d]  dL/dO
+ *   dq, dk, dv: out, bf16 [B,H,N,d]  dL/dQ, dL/dK, dL/dV
+ *   workspace : device scratch of at least fa_bwd_workspace_size() bytes,
+ *               16-byte aligned, owned by the caller; its contents on entry
+ *               do not matter and on return are unspecified.
+ * dQ is accumulated in fp32 across key tiles, then scaled and rounded once.
+ * Calls that share a workspace must not overlap in time (same stream is fine).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk,
+                 void* dv, void* workspace, size_t workspace_bytes, int B,
+                 int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Synchronises `stream`, then reports (and clears) the device status record
+ * of the current GPU: FA_ERR_DEVICE_TIMEOUT if any kernel of this library
+ * gave up on a pipeline wait since the last check, FA_ERR_CUDA if the stream
+ * reported an error, else FA_OK.
+ */
+fa_status fa_check_device_status(void* stream);
+
+/*
+ * Time limit, in nanoseconds, of every pipeline wait inside the kernels
+ * launched after this call (default 2e9 = 2 s).  A wait that runs past it
+ * records FA_ERR_DEVICE_TIMEOUT, stops its thread block cleanly (in-flight
+ * copies drained, tensor memory released) and makes the other blocks of the
+ * grid stop at their next wait.  Values of 0 restore the default.
+ */
+void fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Launches one small kernel whose thread waits, with the configured time
+ * limit, on a pipeline barrier that nothing ever signals, so that the wait
+ * runs out and the failure path of every kernel (status record, clean exit)
+ * can be exercised without harming the GPU.  Used by the test suite; expect
+ * fa_check_device_status() to return FA_ERR_DEVICE_TIMEOUT afterwards.
+ */
+fa_status fa_debug_expire_wait(void* stream);
+
+/*
+ * Measurement hook.  Until called again, every fa_bwd on the calling thread
+ * records the caller-owned CUDA events `before_main` and `after_main`
+ * (cudaEvent_t passed as void*) on its stream immediately before and after
+ * the launch of its main kernel (the one running the tensor-core work), so
+ * the caller can time that kernel alone.  NULL, NULL turns it off.
+ */
+void fa_bwd_set_phase_events(void* before_main, void* after_main);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -17,6 +17,9 @@ What each function follows:
   fwd_online  -- the same result by the running-max / running-sum update of
                  "RTX Flash Attention Implementation COMPLETE", "Online
                  Softmax Algorithm", over key tiles, optionally lazy.
+  fwd_rows, bwd_rows -- the same computations restricted to a range of
+                 query rows (rows are independent), so that long sequences can
+                 be checked on rows the oracle finishes quickly.
   bwd         -- gradients dQ, dK, dV of L with dL/dO = dout, P recomputed
                  from the row's LSE ("GPU Performance Optimization Batch 1 --
                  Design Spec", Item 3, backward paragraph).  The formulas come
@@ -52,6 +55,14 @@ def _load():
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64,
                                    ctypes.c_int, ctypes.c_double, dp, dp, dp]
         lib.oracle_bwd.restype = None
+        lib.oracle_fwd_rows.argtypes = [dp, dp, dp, i64, i64, i64,
+                                        ctypes.c_int, ctypes.c_double, i64,
+                                        i64, dp, dp]
+        lib.oracle_fwd_rows.restype = None
+        lib.oracle_bwd_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64,
+                                        ctypes.c_int, ctypes.c_double, i64,
+                                        i64, dp, dp, dp]
+        lib.oracle_bwd_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -118,4 +129,35 @@ def bwd(q, k, v, dout, causal: bool, scale: float):
     _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), BH, N, d,
                        int(bool(causal)), float(scale), _ptr(dq), _ptr(dk),
                        _ptr(dv))
+    return dq, dk, dv
+
+
+def fwd_rows(q, k, v, causal: bool, scale: float, r0: int, r1: int):
+    """Forward for query rows r0 <= i < r1 only; other rows are NaN."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    BH, N, d = _shape(q)
+    if not 0 <= r0 <= r1 <= N:
+        raise ValueError("bad row range")
+    o = np.full_like(q, np.nan)
+    lse = np.full(q.shape[:-1], np.nan, dtype=np.float64)
+    _load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), BH, N, d,
+                            int(bool(causal)), float(scale), int(r0), int(r1),
+                            _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def bwd_rows(q, k, v, dout, causal: bool, scale: float, r0: int, r1: int):
+    """Backward contributions of query rows r0 <= i < r1 only.  dQ is exact on
+    those rows; dK/dV are partial sums over those rows (exact for keys
+    j >= r0 when causal and r1 == N)."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    BH, N, d = _shape(q)
+    if not 0 <= r0 <= r1 <= N:
+        raise ValueError("bad row range")
+    dq = np.empty_like(q)
+    dk = np.empty_like(q)
+    dv = np.empty_like(q)
+    _load().oracle_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), BH, N, d,
+                            int(bool(causal)), float(scale), int(r0), int(r1),
+                            _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv

@@ -81,10 +81,13 @@ static double row_scores_lse(const double* qi, const double* k, int64_t nvis,
 /*
  * Forward.  q, k, v, o: [BH, N, d] row-major doubles; lse: [BH, N].
  * P_ij = exp(s_ij - lse_i); O_i = sum_j P_ij v_j.
+ * The _rows variant computes only query rows r0 <= i < r1 (each row is
+ * independent) and leaves the other rows of o and lse untouched.
  */
-void oracle_fwd(const double* q, const double* k, const double* v,
-                int64_t BH, int64_t N, int64_t d, int causal, double scale,
-                double* o, double* lse) {
+void oracle_fwd_rows(const double* q, const double* k, const double* v,
+                     int64_t BH, int64_t N, int64_t d, int causal,
+                     double scale, int64_t r0, int64_t r1, double* o,
+                     double* lse) {
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
@@ -94,7 +97,7 @@ void oracle_fwd(const double* q, const double* k, const double* v,
       const double* kh = k + bh * N * d;
       const double* vh = v + bh * N * d;
       double* oh = o + bh * N * d;
-      for (int64_t i = 0; i < N; ++i) {
+      for (int64_t i = r0; i < r1; ++i) {
         int64_t nvis = visible_keys(i, N, causal);
         double l = row_scores_lse(qh + i * d, kh, nvis, d, scale, s);
         lse[bh * N + i] = l;
@@ -109,6 +112,12 @@ void oracle_fwd(const double* q, const double* k, const double* v,
     }
     free(s);
   }
+}
+
+void oracle_fwd(const double* q, const double* k, const double* v,
+                int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                double* o, double* lse) {
+  oracle_fwd_rows(q, k, v, BH, N, d, causal, scale, 0, N, o, lse);
 }
 
 /*
@@ -178,10 +187,15 @@ void oracle_fwd_online(const double* q, const double* k, const double* v,
  * O_i = sum_j P_ij v_j, D_i = dO_i . O_i; then for each visible key j:
  *   dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
  *   dQ_i += scale dS_ij k_j,  dK_j += scale dS_ij q_i,  dV_j += P_ij dO_i.
+ * The _rows variant sums the contributions of query rows r0 <= i < r1 only:
+ * dq is exact on those rows (zero elsewhere); dk and dv hold the partial sums
+ * over those rows, which are the full gradients for keys j >= r0 when causal
+ * and r1 = N (no other row sees such a key).
  */
-void oracle_bwd(const double* q, const double* k, const double* v,
-                const double* dout, int64_t BH, int64_t N, int64_t d,
-                int causal, double scale, double* dq, double* dk, double* dv) {
+void oracle_bwd_rows(const double* q, const double* k, const double* v,
+                     const double* dout, int64_t BH, int64_t N, int64_t d,
+                     int causal, double scale, int64_t r0, int64_t r1,
+                     double* dq, double* dk, double* dv) {
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
@@ -198,7 +212,7 @@ void oracle_bwd(const double* q, const double* k, const double* v,
       memset(dqh, 0, sizeof(double) * (size_t)(N * d));
       memset(dkh, 0, sizeof(double) * (size_t)(N * d));
       memset(dvh, 0, sizeof(double) * (size_t)(N * d));
-      for (int64_t i = 0; i < N; ++i) {
+      for (int64_t i = r0; i < r1; ++i) {
         int64_t nvis = visible_keys(i, N, causal);
         const double* qi = qh + i * d;
         const double* doi = doh + i * d;
@@ -230,4 +244,10 @@ void oracle_bwd(const double* q, const double* k, const double* v,
     free(oi);
     free(s);
   }
+}
+
+void oracle_bwd(const double* q, const double* k, const double* v,
+                const double* dout, int64_t BH, int64_t N, int64_t d,
+                int causal, double scale, double* dq, double* dk, double* dv) {
+  oracle_bwd_rows(q, k, v, dout, BH, N, d, causal, scale, 0, N, dq, dk, dv);
 }

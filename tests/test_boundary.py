@@ -1,0 +1,123 @@
+"""The C-ABI library on the host (CPU only, no GPU calls).
+
+Checks that libfa.so builds for sm_103a, loads, exports every function that
+include/fa.h declares, and rejects bad arguments on the host before anything
+would reach a GPU.  Every call here returns before the library's first CUDA
+runtime call.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from tiled_attention_bwd_gb300 import build as fa_build
+from tiled_attention_bwd_gb300 import fa
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def test_header_declares_the_expected_entry_points():
+    names = fa.header_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
+              "fa_check_device_status", "fa_status_string",
+              "fa_set_wait_timeout_ns", "fa_debug_expire_wait"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in fa.header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_library_targets_sm103a():
+    out = subprocess.run(["cuobjdump", "--list-elf", fa.LIB_PATH],
+                         capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_missing_library_fails_loudly():
+    with pytest.raises(RuntimeError):
+        fa.open_library("/nonexistent/libfa.so")
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS_NAMES.items():
+        assert lib.fa_status_string(code).decode() == name
+    assert lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, N=128, d=128,
+         causal=0, scale=0.125):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_fwd(p(q), p(k), p(v), p(o), p(lse), B, H, N, d, causal,
+                      scale, None)
+
+
+def _bwd(lib, ptr=16, ws=16, ws_bytes=1 << 40, B=1, H=1, N=128, d=128,
+         causal=0, scale=0.125, lse=16):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_bwd(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), p(ptr), p(ptr),
+                      p(ptr), p(ptr), p(ws), ws_bytes, B, H, N, d, causal,
+                      scale, None)
+
+
+def test_forward_argument_checks(lib):
+    assert _fwd(lib, d=96) == UNSUPPORTED
+    assert _fwd(lib, d=256) == UNSUPPORTED
+    assert _fwd(lib, d=0) == INVALID
+    assert _fwd(lib, scale=0.0) == INVALID
+    assert _fwd(lib, scale=-1.0) == INVALID
+    assert _fwd(lib, scale=float("inf")) == INVALID
+    assert _fwd(lib, scale=float("nan")) == INVALID
+    assert _fwd(lib, causal=2) == INVALID
+    assert _fwd(lib, B=-1) == INVALID
+    assert _fwd(lib, N=65535 * 128 + 1) == UNSUPPORTED
+    assert _fwd(lib, q=0) == INVALID            # null pointer
+    assert _fwd(lib, lse=0) == INVALID
+    assert _fwd(lib, q=24) == INVALID           # not 16-byte aligned
+    assert _fwd(lib, o=8) == INVALID
+    assert _fwd(lib, lse=18) == INVALID         # not 4-byte aligned
+
+
+def test_empty_problems_are_no_ops(lib):
+    # No element to compute: FA_OK without touching (here: null) pointers.
+    assert _fwd(lib, q=0, k=0, v=0, o=0, lse=0, N=0) == OK
+    assert _fwd(lib, q=0, k=0, v=0, o=0, lse=0, B=0) == OK
+    assert _bwd(lib, ptr=0, ws=0, ws_bytes=0, lse=0, H=0) == OK
+    assert lib.fa_bwd_workspace_size(0, 4, 128, 128) == 0
+
+
+def test_backward_argument_checks(lib):
+    assert _bwd(lib, d=80) == UNSUPPORTED
+    assert _bwd(lib, scale=0.0) == INVALID
+    assert _bwd(lib, ptr=0) == INVALID
+    assert _bwd(lib, ptr=40) == INVALID
+    assert _bwd(lib, ws=0) == WORKSPACE
+    assert _bwd(lib, ws=8) == WORKSPACE
+    need = lib.fa_bwd_workspace_size(1, 1, 128, 128)
+    assert _bwd(lib, ws_bytes=need - 1) == WORKSPACE
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 8, 512, 64), (4, 64, 4096, 128),
+                                     (1, 1, 1, 64), (3, 5, 333, 128)])
+def test_workspace_size(lib, B, H, N, d):
+    n_pad = _align(N, 128)
+    expect = (_align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4))
+    assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == expect

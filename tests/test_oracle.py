@@ -225,3 +225,32 @@ def test_gradient_invariants(causal):
 
 def test_thread_count_is_reported():
     assert oracle.num_threads() >= 1
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_ranges_agree_with_full_computation(causal):
+    shape = (1, 2, 90, 8)
+    q, k, v, do = (_rand(shape, 110 + s) for s in range(4))
+    o, lse = oracle.fwd(q, k, v, causal, 0.3)
+    dq, dk, dv = oracle.bwd(q, k, v, do, causal, 0.3)
+    parts = [(0, 17), (17, 60), (60, 90)]
+    sum_dk = np.zeros(shape)
+    sum_dv = np.zeros(shape)
+    for r0, r1 in parts:
+        o_r, lse_r = oracle.fwd_rows(q, k, v, causal, 0.3, r0, r1)
+        np.testing.assert_allclose(o_r[:, :, r0:r1], o[:, :, r0:r1], atol=1e-15)
+        np.testing.assert_allclose(lse_r[:, :, r0:r1], lse[:, :, r0:r1], atol=1e-15)
+        assert np.isnan(o_r[:, :, :r0]).all() and np.isnan(o_r[:, :, r1:]).all()
+        dq_r, dk_r, dv_r = oracle.bwd_rows(q, k, v, do, causal, 0.3, r0, r1)
+        np.testing.assert_allclose(dq_r[:, :, r0:r1], dq[:, :, r0:r1], atol=1e-14)
+        assert np.all(dq_r[:, :, :r0] == 0) and np.all(dq_r[:, :, r1:] == 0)
+        sum_dk += dk_r
+        sum_dv += dv_r
+    # Contributions of disjoint row ranges add up to the full gradients.
+    np.testing.assert_allclose(sum_dk, dk, atol=1e-13)
+    np.testing.assert_allclose(sum_dv, dv, atol=1e-13)
+    if causal:
+        # Keys j >= r0 are seen only by rows i >= r0.
+        _, dk_t, dv_t = oracle.bwd_rows(q, k, v, do, True, 0.3, 60, 90)
+        np.testing.assert_allclose(dk_t[:, :, 60:], dk[:, :, 60:], atol=1e-14)
+        np.testing.assert_allclose(dv_t[:, :, 60:], dv[:, :, 60:], atol=1e-14)

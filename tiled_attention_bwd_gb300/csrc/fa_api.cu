@@ -1,0 +1,304 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
+// checks, TMA descriptor encoding, launch sequencing, the per-GPU device
+// status record, and the wait-expiry self-test kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_common.cuh"
+#include "fa_launch.h"
+
+namespace {
+
+__device__ fa::DevState g_dev_state;  // zero-initialised at module load
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxN = 65535 * fa::kTile;  // grid.y limit of the key-tile grid
+
+struct DeviceCtx {
+  bool ready = false;
+  fa::DevState* state = nullptr;
+  int sm_count = 0;
+};
+DeviceCtx g_ctx[kMaxDevices];
+std::mutex g_ctx_mu;
+
+thread_local cudaEvent_t g_ev_before_main = nullptr;
+thread_local cudaEvent_t g_ev_after_main = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Per-device set-up: device address of the status record, SM count.
+fa_status device_ctx(DeviceCtx** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ctx_mu);
+  DeviceCtx& c = g_ctx[dev];
+  if (!c.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_state) != cudaSuccess) return FA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    c.state = static_cast<fa::DevState*>(p);
+    c.sm_count = sms;
+    c.ready = true;
+  }
+  *out = &c;
+  return FA_OK;
+}
+
+fa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!g_encode) return FA_ERR_CUDA;
+  *fn = g_encode;
+  return FA_OK;
+}
+
+// 3-D view [BH][N][d] of a bf16 [B,H,N,d] tensor; box = 128 rows x 64 columns
+// (128 bytes, the swizzle width).  Rows past N read as zeros.
+fa_status make_tile_map(CUtensorMap* m, const void* base, int BH, int N,
+                        int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  fa_status s = encode_fn(&fn);
+  if (s != FA_OK) return s;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Shared shape/scalar checks.  *empty is set for a problem with no elements.
+fa_status check_shape(int B, int H, int N, int d, int causal, float scale,
+                      bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (d <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H > INT_MAX) return FA_ERR_UNSUPPORTED;
+  if (N > kMaxN) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) *empty = true;
+  return FA_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t dq_acc_off, ddot_off, lse2_off, total;
+};
+
+WsLayout ws_layout(int B, int H, int N, int d) {
+  const size_t BH = (size_t)B * H;
+  const size_t n_pad = align_up((size_t)N, fa::kTile);
+  WsLayout w;
+  w.dq_acc_off = 0;
+  w.ddot_off = align_up(BH * N * d * sizeof(float), 256);
+  w.lse2_off = w.ddot_off + align_up(BH * n_pad * sizeof(float), 256);
+  w.total = w.lse2_off + align_up(BH * n_pad * sizeof(float), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+void fa_set_wait_timeout_ns(uint64_t ns) {
+  g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
+                 float* lse, int B, int H, int N, int d, int causal,
+                 float scale, void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  DeviceCtx* ctx = nullptr;
+  if ((s = device_ctx(&ctx)) != FA_OK) return s;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tk, k, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  fa::FwdArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.N = N;
+  a.scale_log2 = scale * fa::kLog2e;
+  a.st = ctx->state;
+  a.timeout_ns = g_timeout_ns.load();
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
+  return ws_layout(B, H, N, d).total;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk,
+                 void* dv, void* workspace, size_t workspace_bytes, int B,
+                 int H, int N, int d, int causal, float scale, void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(B, H, N, d);
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  DeviceCtx* ctx = nullptr;
+  if ((s = device_ctx(&ctx)) != FA_OK) return s;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tk, k, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tdo, dout, BH, N, d)) != FA_OK) return s;
+  char* ws = static_cast<char*>(workspace);
+  fa::BwdArgs a{};
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.lse = lse;
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
+  a.ddot = reinterpret_cast<float*>(ws + w.ddot_off);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.BH = BH;
+  a.N = N;
+  a.N_pad = (int)align_up((size_t)N, fa::kTile);
+  a.scale = scale;
+  a.scale_log2 = scale * fa::kLog2e;
+  a.st = ctx->state;
+  a.timeout_ns = g_timeout_ns.load();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int elem_blocks = ctx->sm_count * 8;
+  cudaError_t e = fa::launch_bwd_pre(a, d, elem_blocks, st);
+  if (e == cudaSuccess && g_ev_before_main)
+    e = cudaEventRecord(g_ev_before_main, st);
+  if (e == cudaSuccess)
+    e = fa::launch_bwd_main(tq, tk, tv, tdo, a, d, causal != 0, st);
+  if (e == cudaSuccess && g_ev_after_main)
+    e = cudaEventRecord(g_ev_after_main, st);
+  if (e == cudaSuccess) e = fa::launch_bwd_post(a, d, elem_blocks, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+void fa_bwd_set_phase_events(void* before_main, void* after_main) {
+  g_ev_before_main = static_cast<cudaEvent_t>(before_main);
+  g_ev_after_main = static_cast<cudaEvent_t>(after_main);
+}
+
+fa_status fa_check_device_status(void* stream) {
+  DeviceCtx* ctx = nullptr;
+  fa_status s = device_ctx(&ctx);
+  if (s != FA_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  fa::DevState h{};
+  if (cudaMemcpy(&h, ctx->state, sizeof(h), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  if (h.status == 0 && h.abort == 0) return FA_OK;
+  if (cudaMemset(ctx->state, 0, sizeof(fa::DevState)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  return h.status != 0 ? static_cast<fa_status>(h.status)
+                       : FA_ERR_DEVICE_TIMEOUT;
+}
+
+fa_status fa_debug_expire_wait(void* stream) {
+  DeviceCtx* ctx = nullptr;
+  fa_status s = device_ctx(&ctx);
+  if (s != FA_OK) return s;
+  cudaError_t e = fa::launch_expire_wait(ctx->state, g_timeout_ns.load(),
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace fa {
+
+// One thread waits, with the configured limit, on a barrier whose single
+// expected arrival never happens; the wait expires and records the timeout.
+__global__ void expire_wait_kernel(DevState* st, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t cta_abort;
+  if (threadIdx.x == 0) {
+    cta_abort = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{st, &cta_abort, timeout_ns};
+    (void)wait_bar(&bar, 0, wc, 0x7E57u);
+  }
+}
+
+cudaError_t launch_expire_wait(DevState* st, uint64_t timeout_ns,
+                               cudaStream_t stream) {
+  expire_wait_kernel<<<1, 32, 0, stream>>>(st, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,558 @@
+// fa_bwd.cu -- backward attention kernels for sm_103a.
+//
+// Gradients of O = softmax(scale Q K^T [+ mask]) V with P recomputed from the
+// saved LSE instead of stored ("GPU Performance Optimization Batch 1 -- Design
+// Spec", Item 3, backward paragraph; "RTX Flash Attention Implementation
+// COMPLETE", "Flash Attention Backward Kernel": gradient recomputation,
+// atomic memory operations, dQ/dK/dV updates).  With D_i = dO_i . O_i:
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dQ = scale dS K,
+//   dK = scale dS^T Q.
+//
+// Three launches on one stream:
+//   pre   D_i and LSE_i*log2(e) per row (padded to whole tiles: D = 0 and
+//         LSE2 = +inf past N, which zeroes P there); dQ accumulator := 0.
+//   main  one thread block per (batch, head, 128-key tile j).  K_j, V_j stay
+//         in smem; dK_j, dV_j accumulate in TMEM; Q_i, dO_i stream through a
+//         two-stage TMA ring (causal: only i >= j).  Per Q tile, five tcgen05
+//         MMAs: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P^T from TMEM),
+//         dK += dS^T Q and dQ_i = dS K (dS from smem, read K-major for the
+//         first and MN-major for the second).  dQ_i leaves TMEM as fp32
+//         atomic adds into the accumulator.
+//   post  dQ = scale * accumulator, rounded to bf16.
+//
+// Warps of the main kernel:
+//   0-3  thread = key row: P^T = exp2(S^T c - LSE2), then dS^T = P^T (dP^T - D)
+//   4-7  thread = query row: drain dQ_i from TMEM into global fp32 adds
+//   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
+// TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T and then dQ [128,256)
+// dK [256, 256+d)  dV [256+d, 256+2d).
+#include "fa_common.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kSub = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kStageOff = 2 * kTileBytes;
+  // Q_i, dO_i, LSE2_i[128], D_i[128]
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kTile * 4;
+  static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kDSBytes = kTile * kTile * 2;  // 2 sub-tiles [128][64]
+  static constexpr int kBarOff = kDSOff + kDSBytes;
+  // d = 128 uses 231,680 of the 232,448 bytes a block may have, so the base
+  // is taken as is (checked at run time); d = 64 keeps alignment slack.
+  static constexpr int kSlack = (D == 128) ? 0 : 1024;
+  static constexpr int kSmemBytes = kBarOff + 256 + kSlack;
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t s_full;
+  uint64_t dp_full;
+  uint64_t p_full;
+  uint64_t ds_full;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t ds_free;
+  uint64_t acc_done;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+enum : uint32_t {
+  kWBwdProdEmpty = 0x111,
+  kWBwdMmaKV = 0x211,
+  kWBwdMmaSt = 0x212,
+  kWBwdMmaDqFree = 0x213,
+  kWBwdMmaP = 0x214,
+  kWBwdMmaDs = 0x215,
+  kWBwdCmpSt = 0x311,
+  kWBwdCmpS = 0x312,
+  kWBwdCmpDp = 0x313,
+  kWBwdCmpDsFree = 0x314,
+  kWBwdCmpAcc = 0x315,
+  kWBwdDqFull = 0x411,
+  kWBwdDqAcc = 0x412,
+  kWBwdMisaligned = 0x5A1,
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (L::kSlack > 0) ? align1024(smem_raw) : smem_raw;
+  auto* bars = reinterpret_cast<BwdBars*>(smem + L::kBarOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int j = blockIdx.y;                       // key tile
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  const int i_begin = CAUSAL ? j : 0;             // first query tile
+  const int nq = n_tiles - i_begin;
+
+  if (threadIdx.x == 0) {
+    uint32_t stop = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
+    if ((smem_addr(smem) & 1023u) != 0) {
+      atomicCAS(&a.st->status, 0u, (unsigned)FA_ERR_UNSUPPORTED);
+      atomicExch(&a.st->where, kWBwdMisaligned);
+      stop = 1;
+    }
+    bars->abort = stop;
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->st_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool run = ld_volatile_u32(&bars->abort) == 0;
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{a.st, &bars->abort, a.timeout_ns};
+  uint8_t* const k_s = smem + L::kKOff;
+  uint8_t* const v_s = smem + L::kVOff;
+  uint8_t* const ds_s = smem + L::kDSOff;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && run) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTileBytes);
+#pragma unroll
+      for (int sb = 0; sb < L::kSub; ++sb) {
+        tma_load_3d(k_s + sb * kSubTileBytes, &tm_k, &bars->kv_full, sb * 64,
+                    j * kTile, bh);
+        tma_load_3d(v_s + sb * kSubTileBytes, &tm_v, &bars->kv_full, sb * 64,
+                    j * kTile, bh);
+      }
+      int last_par[2] = {-1, -1};
+      bool ok = true;
+      for (int it = 0; it < nq; ++it) {
+        const int i = i_begin + it;
+        const int stage = it & 1;
+        const uint32_t sp = (uint32_t)((it >> 1) & 1);
+        ok = wait_bar(&bars->st_empty[stage], sp ^ 1u, wc, kWBwdProdEmpty);
+        if (!ok) break;
+        uint8_t* st = smem + L::kStageOff + stage * L::kStageBytes;
+        mbar_arrive_expect_tx(&bars->st_full[stage],
+                              2 * L::kTileBytes + 2 * kTile * 4);
+#pragma unroll
+        for (int sb = 0; sb < L::kSub; ++sb) {
+          tma_load_3d(st + sb * kSubTileBytes, &tm_q, &bars->st_full[stage],
+                      sb * 64, i * kTile, bh);
+          tma_load_3d(st + L::kTileBytes + sb * kSubTileBytes, &tm_do,
+                      &bars->st_full[stage], sb * 64, i * kTile, bh);
+        }
+        const size_t row0 = (size_t)bh * a.N_pad + (size_t)i * kTile;
+        bulk_load(st + 2 * L::kTileBytes, a.lse2 + row0, kTile * 4,
+                  &bars->st_full[stage]);
+        bulk_load(st + 2 * L::kTileBytes + kTile * 4, a.ddot + row0, kTile * 4,
+                  &bars->st_full[stage]);
+        last_par[stage] = (int)sp;
+      }
+      if (!ok) {
+        drain_bar(&bars->kv_full, 0, a.timeout_ns);
+        for (int s = 0; s < 2; ++s)
+          if (last_par[s] >= 0)
+            drain_bar(&bars->st_full[s], (uint32_t)last_par[s], a.timeout_ns);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0 && run) {
+      constexpr uint32_t id_st = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t id_q = idesc_bf16(128, D, true, true);
+      const uint32_t k_a = smem_addr(k_s), v_a = smem_addr(v_s);
+      const uint32_t ds_a = smem_addr(ds_s);
+      const uint32_t tS = tmem, tDP = tmem + 128;
+      const uint32_t tDK = tmem + 256, tDV = tmem + 256 + D;
+      bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
+      for (int it = 0; it < nq && ok; ++it) {
+        const int stage = it & 1;
+        const uint32_t sp = (uint32_t)((it >> 1) & 1);
+        const uint32_t par = (uint32_t)(it & 1);
+        ok = wait_bar(&bars->st_full[stage], sp, wc, kWBwdMmaSt);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t q_a = smem_addr(smem + L::kStageOff + stage * L::kStageBytes);
+        const uint32_t do_a = q_a + L::kTileBytes;
+        // S^T = K_j Q_i^T   [keys x queries], K = d
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
+          mma_ss(tS, sdesc_sw128(k_a + off, 16, 1024),
+                 sdesc_sw128(q_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full);
+        if (it > 0) {
+          // dQ_{i-1} sits in the dP columns until drained.
+          ok = wait_bar(&bars->dq_free, par ^ 1u, wc, kWBwdMmaDqFree);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dP^T = V_j dO_i^T   [keys x queries], K = d
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
+          mma_ss(tDP, sdesc_sw128(v_a + off, 16, 1024),
+                 sdesc_sw128(do_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dp_full);
+        ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
+        if (!ok) break;
+        tc_fence_after();
+        // dV_j += P^T dO_i   [keys x d], K = queries; P^T from TMEM
+#pragma unroll
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_ts(tDV, tS + s * 8,
+                 sdesc_sw128(do_a + s * 2048, kSubTileBytes, 1024), id_kv,
+                 (it > 0 || s > 0) ? 1u : 0u);
+        ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
+        if (!ok) break;
+        tc_fence_after();
+        // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T K-major in smem
+#pragma unroll
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_ss(tDK,
+                 sdesc_sw128(ds_a + (s >> 2) * kSubTileBytes + (s & 3) * 32, 16,
+                             1024),
+                 sdesc_sw128(q_a + s * 2048, kSubTileBytes, 1024), id_kv,
+                 (it > 0 || s > 0) ? 1u : 0u);
+        // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
+#pragma unroll
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_ss(tDP, sdesc_sw128(ds_a + s * 2048, kSubTileBytes, 1024),
+                 sdesc_sw128(k_a + s * 2048, kSubTileBytes, 1024), id_q,
+                 s > 0 ? 1u : 0u);
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->st_empty[stage]);
+        mma_commit(&bars->ds_free);
+      }
+      if (ok) mma_commit(&bars->acc_done);
+      mma_commit(&bars->mma_done);
+      drain_bar(&bars->mma_done, 0, a.timeout_ns);
+    }
+  } else if (warp < 4) {
+    // -------------------------------------- P^T and dS^T (thread = key row)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                  // key row in tile j
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const float c = a.scale_log2;
+    bool ok = run;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int i = i_begin + it;
+      const int stage = it & 1;
+      const uint32_t sp = (uint32_t)((it >> 1) & 1);
+      const uint32_t par = (uint32_t)(it & 1);
+      ok = wait_bar_warp(&bars->st_full[stage], sp, wc, kWBwdCmpSt);
+      if (!ok) break;
+      const float* lse2 = reinterpret_cast<const float*>(
+          smem + L::kStageOff + stage * L::kStageBytes + 2 * L::kTileBytes);
+      const float* dd = lse2 + kTile;
+      ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tl + 0, s);
+      tmem_ld32(tl + 32, s + 32);
+      tmem_ld32(tl + 64, s + 64);
+      tmem_ld32(tl + 96, s + 96);
+      tmem_wait_ld();
+      reg_fence32(s);
+      reg_fence32(s + 32);
+      reg_fence32(s + 64);
+      reg_fence32(s + 96);
+      uint32_t pk[64];
+      const bool diag = CAUSAL && (i == j);
+#pragma unroll
+      for (int e = 0; e < 128; e += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + e);
+        float x0 = fmaf(__uint_as_float(s[e + 0]), c, -l4.x);
+        float x1 = fmaf(__uint_as_float(s[e + 1]), c, -l4.y);
+        float x2 = fmaf(__uint_as_float(s[e + 2]), c, -l4.z);
+        float x3 = fmaf(__uint_as_float(s[e + 3]), c, -l4.w);
+        if (diag) {  // query e < key r is masked
+          if (e + 0 < r) x0 = -INFINITY;
+          if (e + 1 < r) x1 = -INFINITY;
+          if (e + 2 < r) x2 = -INFINITY;
+          if (e + 3 < r) x3 = -INFINITY;
+        }
+        pk[e / 2] = pack_bf16(ex2(x0), ex2(x1));
+        pk[e / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
+      }
+      tmem_st32(tl + 0, pk);
+      tmem_st32(tl + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+
+      ok = wait_bar_warp(&bars->dp_full, par, wc, kWBwdCmpDp);
+      if (ok && it > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t dp[32];
+        tmem_ld32(tl + 128 + ch * 32, dp);
+        tmem_wait_ld();
+        reg_fence32(dp);
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int q = ch * 32 + e;
+          const float4 d4 = *reinterpret_cast<const float4*>(dd + q);
+          const uint32_t pa = pk[q / 2], pb = pk[q / 2 + 1];
+          const float ds0 = bf16_lo(pa) * (__uint_as_float(dp[e + 0]) - d4.x);
+          const float ds1 = bf16_hi(pa) * (__uint_as_float(dp[e + 1]) - d4.y);
+          const float ds2 = bf16_lo(pb) * (__uint_as_float(dp[e + 2]) - d4.z);
+          const float ds3 = bf16_hi(pb) * (__uint_as_float(dp[e + 3]) - d4.w);
+          dsk[e / 2] = pack_bf16(ds0, ds1);
+          dsk[e / 2 + 1] = pack_bf16(ds2, ds3);
+        }
+        // Row r of dS^T, queries ch*32 .. ch*32+31, into the swizzled tile.
+        uint8_t* sub = ds_s + (ch >> 1) * kSubTileBytes;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t col = (uint32_t)((ch & 1) * 32 + g * 8);
+          *reinterpret_cast<uint4*>(sub + sw128_offset((uint32_t)r, col)) =
+              make_uint4(dsk[4 * g], dsk[4 * g + 1], dsk[4 * g + 2],
+                         dsk[4 * g + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+    }
+    // dK epilogue (rows = keys)
+    if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdCmpAcc);
+    if (ok) {
+      tc_fence_after();
+      const int krow = j * kTile + r;
+      const bool valid = krow < a.N;
+      __nv_bfloat16* out = a.dk + ((size_t)bh * a.N + (valid ? krow : 0)) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tl + 256 + ch * 32, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        uint32_t pkv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pkv[e] = pack_bf16(__uint_as_float(v[2 * e]) * a.scale,
+                             __uint_as_float(v[2 * e + 1]) * a.scale);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
+                                 pkv[4 * v4 + 3]);
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------- dQ drain (thread = query row)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    bool ok = run;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int i = i_begin + it;
+      ok = wait_bar_warp(&bars->dq_full, (uint32_t)(it & 1), wc, kWBwdDqFull);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[D];
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tl + 128 + ch * 32, acc + ch * 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) reg_fence32(acc + ch * 32);
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
+      const int q = i * kTile + r;
+      if (q < a.N) {
+        float4* dst = reinterpret_cast<float4*>(a.dq_acc + ((size_t)bh * a.N + q) * D);
+#pragma unroll
+        for (int v4 = 0; v4 < D / 4; ++v4)
+          atomicAdd(dst + v4, make_float4(__uint_as_float(acc[4 * v4]),
+                                          __uint_as_float(acc[4 * v4 + 1]),
+                                          __uint_as_float(acc[4 * v4 + 2]),
+                                          __uint_as_float(acc[4 * v4 + 3])));
+      }
+    }
+    // dV epilogue (rows = keys)
+    if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdDqAcc);
+    if (ok) {
+      tc_fence_after();
+      const int krow = j * kTile + r;
+      const bool valid = krow < a.N;
+      __nv_bfloat16* out = a.dv + ((size_t)bh * a.N + (valid ? krow : 0)) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tl + 256 + D + ch * 32, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        uint32_t pkv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pkv[e] = pack_bf16(__uint_as_float(v[2 * e]),
+                             __uint_as_float(v[2 * e + 1]));
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
+                                 pkv[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D_i = dO_i . O_i and LSE2_i = LSE_i log2(e) for every padded row (one warp
+// per row); then the dQ accumulator is cleared.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long warps_total = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long rows = (long long)a.BH * a.N_pad;
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < rows; row += warps_total) {
+    const int bh = (int)(row / a.N_pad);
+    const int q = (int)(row % a.N_pad);
+    float dsum = 0.f, l2 = INFINITY;
+    if (q < a.N) {
+      const size_t base = ((size_t)bh * a.N + q) * D;
+      constexpr int kPer = D / 32;  // 4 (d=128) or 2 (d=64) elements per lane
+      if constexpr (kPer == 4) {
+        const uint2 ov = *reinterpret_cast<const uint2*>(a.o + base + lane * 4);
+        const uint2 dv = *reinterpret_cast<const uint2*>(a.dout + base + lane * 4);
+        dsum = bf16_lo(ov.x) * bf16_lo(dv.x) + bf16_hi(ov.x) * bf16_hi(dv.x) +
+               bf16_lo(ov.y) * bf16_lo(dv.y) + bf16_hi(ov.y) * bf16_hi(dv.y);
+      } else {
+        const uint32_t ov = *reinterpret_cast<const uint32_t*>(a.o + base + lane * 2);
+        const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dout + base + lane * 2);
+        dsum = bf16_lo(ov) * bf16_lo(dv) + bf16_hi(ov) * bf16_hi(dv);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+      l2 = a.lse[(size_t)bh * a.N + q] * kLog2e;
+    }
+    if (lane == 0) {
+      a.ddot[row] = dsum;
+      a.lse2[row] = l2;
+    }
+  }
+  const long long n4 = (long long)a.BH * a.N * D / 4;
+  float4* acc = reinterpret_cast<float4*>(a.dq_acc);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n4;
+       idx += (long long)gridDim.x * blockDim.x)
+    acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = scale * accumulator -> bf16, eight elements per thread per step.
+__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
+  const long long n8 = (long long)a.BH * a.N * d / 8;
+  const float4* acc = reinterpret_cast<const float4*>(a.dq_acc);
+  uint4* out = reinterpret_cast<uint4*>(a.dq);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const float4 x = acc[2 * idx], y = acc[2 * idx + 1];
+    out[idx] = make_uint4(pack_bf16(x.x * a.scale, x.y * a.scale),
+                          pack_bf16(x.z * a.scale, x.w * a.scale),
+                          pack_bf16(y.x * a.scale, y.y * a.scale),
+                          pack_bf16(y.z * a.scale, y.w * a.scale));
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const BwdArgs& a, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto kern = bwd_main_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  dim3 grid((unsigned)a.BH, (unsigned)n_tiles);
+  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
+                           cudaStream_t stream) {
+  if (d == 128)
+    bwd_pre_kernel<128><<<grid_blocks, 256, 0, stream>>>(a);
+  else
+    bwd_pre_kernel<64><<<grid_blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const BwdArgs& a, int d, bool causal,
+                            cudaStream_t stream) {
+  if (d == 128)
+    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, a, stream)
+                  : launch_main_t<128, false>(tq, tk, tv, tdo, a, stream);
+  return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, a, stream)
+                : launch_main_t<64, false>(tq, tk, tv, tdo, a, stream);
+}
+
+cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
+                            cudaStream_t stream) {
+  bwd_post_kernel<<<grid_blocks, 256, 0, stream>>>(a, d);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

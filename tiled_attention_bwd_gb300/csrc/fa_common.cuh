@@ -1,0 +1,112 @@
+// fa_common.cuh -- pieces shared by the forward and backward kernels:
+// the device status record, bounded pipeline waits, tile geometry.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kTile = 128;            // rows of a Q tile and of a K/V tile
+constexpr int kSwizzleBytes = 128;    // width of one swizzled smem row
+constexpr int kSubTileBytes = kTile * kSwizzleBytes;  // 128 rows x 64 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One per GPU, in device memory owned by the library.  `status` keeps the
+// first error code, `abort` tells every running block to stop at its next
+// wait, `where` records which wait expired (role * 256 + site).
+struct DevState {
+  unsigned int status;
+  unsigned int abort;
+  unsigned int where;
+  unsigned int blocks_aborted;
+};
+
+// Everything a bounded wait needs.
+struct WaitCtl {
+  DevState* st;
+  uint32_t* cta_abort;  // shared-memory flag: this block is stopping
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+
+__device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t where) {
+  atomicCAS(&c.st->status, 0u, (unsigned)FA_ERR_DEVICE_TIMEOUT);
+  atomicExch(&c.st->where, where);
+  atomicExch(&c.st->abort, 1u);
+  atomicAdd(&c.st->blocks_aborted, 1u);
+  *reinterpret_cast<volatile uint32_t*>(c.cta_abort) = 1u;
+}
+
+// Wait for the phase of `bar` with the given parity.  Returns false (and
+// never blocks longer than the time limit) if the wait expired here or the
+// block / grid is already stopping.
+static __device__ __noinline__ bool wait_bar_slow(uint64_t* bar,
+                                                   uint32_t parity,
+                                                   WaitCtl c, uint32_t where) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (ld_volatile_u32(c.cta_abort)) return false;
+    if (*reinterpret_cast<volatile unsigned int*>(&c.st->abort)) {
+      *reinterpret_cast<volatile uint32_t*>(c.cta_abort) = 1u;
+      return false;
+    }
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      raise_abort(c, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
+                                         const WaitCtl& c, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, c, where);
+}
+
+// Drain wait used only while a block is stopping: waits for an in-flight copy
+// or MMA (which complete on their own) with a time limit, ignoring the abort
+// flags.  Returns false if even that expired.
+static __device__ __noinline__ bool drain_bar(uint64_t* bar, uint32_t parity,
+                                       uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// Warp-uniform wait: every lane waits, and the warp proceeds only if all
+// lanes saw the phase complete (so warp-collective tcgen05 loads/stores are
+// never executed by a partial warp).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity,
+                                              const WaitCtl& c,
+                                              uint32_t where) {
+  bool ok = wait_bar(bar, parity, c, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Aligns the dynamic shared memory base to 1024 bytes (128-byte swizzle atoms).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
+}
+
+// Byte offset of bf16 element (row, col) inside a [128 x 64] tile stored with
+// the 128-byte swizzle (16-byte chunk index XOR row % 8), as TMA writes it.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
+  uint32_t chunk = (col >> 3) ^ (row & 7u);
+  return row * 128u + chunk * 16u + (col & 7u) * 2u;
+}
+
+}  // namespace fa

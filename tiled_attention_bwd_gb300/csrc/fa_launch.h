@@ -1,0 +1,56 @@
+// fa_launch.h -- internal interface between the host layer (fa_api.cu) and
+// the kernel translation units (fa_fwd.cu, fa_bwd.cu).  Not part of the ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+struct DevState;
+
+struct FwdArgs {
+  __nv_bfloat16* o;     // [BH, N, d]
+  float* lse;           // [BH, N]
+  int N;
+  float scale_log2;     // scale * log2(e): scores enter exp2 directly
+  DevState* st;
+  uint64_t timeout_ns;
+};
+
+struct BwdArgs {
+  const __nv_bfloat16* o;     // [BH, N, d]
+  const __nv_bfloat16* dout;  // [BH, N, d]
+  const float* lse;           // [BH, N]
+  float* dq_acc;              // [BH, N, d]  fp32 workspace
+  float* ddot;                // [BH, N_pad] D_i = dO_i . O_i  (0 past N)
+  float* lse2;                // [BH, N_pad] LSE_i * log2(e)   (+inf past N)
+  __nv_bfloat16* dq;          // [BH, N, d]
+  __nv_bfloat16* dk;          // [BH, N, d]
+  __nv_bfloat16* dv;          // [BH, N, d]
+  int BH;
+  int N;
+  int N_pad;                  // N rounded up to a multiple of 128
+  float scale;
+  float scale_log2;
+  DevState* st;
+  uint64_t timeout_ns;
+};
+
+// Each returns the launch error (cudaSuccess on success).
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
+                       bool causal, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const BwdArgs& a, int d, bool causal,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
+                            cudaStream_t stream);
+cudaError_t launch_expire_wait(DevState* st, uint64_t timeout_ns,
+                               cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,191 @@
+"""Python binding of libfa.so (argument marshalling only).
+
+Every function here checks tensor shapes/dtypes/devices, then passes raw
+device pointers and the current CUDA stream to the C ABI of ``include/fa.h``.
+All arithmetic runs in the library's CUDA kernels; there is no fallback.  If
+the library has not been built, loading it raises immediately.
+
+Names mirror the C ABI: ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``,
+``fa_check_device_status``, ``fa_set_wait_timeout_ns``,
+``fa_debug_expire_wait``, ``fa_bwd_set_phase_events``, ``fa_status_string``.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libfa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
+                3: "FA_ERR_CUDA", 4: "FA_ERR_DEVICE_TIMEOUT",
+                5: "FA_ERR_WORKSPACE"}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A non-OK status from libfa.so."""
+
+    def __init__(self, where, status):
+        self.status = int(status)
+        super().__init__("%s failed: %s (%d)" % (
+            where, STATUS_NAMES.get(self.status, "FA_ERR_UNKNOWN"),
+            self.status))
+
+
+def load_library():
+    """Load the in-tree libfa.so (once).  Raises if it is missing: there is
+    no other compute path."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(LIB_PATH)
+    return _lib
+
+
+def open_library(path: str):
+    """Open a libfa.so at `path` and declare its C signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "libfa.so not found at %s; build it with "
+            "`python -m tiled_attention_bwd_gb300.build`" % path)
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                           ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_check_device_status.argtypes = [vp]
+    lib.fa_check_device_status.restype = i
+    lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_set_wait_timeout_ns.restype = None
+    lib.fa_debug_expire_wait.argtypes = [vp]
+    lib.fa_debug_expire_wait.restype = i
+    lib.fa_bwd_set_phase_events.argtypes = [vp, vp]
+    lib.fa_bwd_set_phase_events.restype = None
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def header_functions(path: str = HEADER_PATH):
+    """Names of the functions declared in include/fa.h."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(where, status):
+    if status != FA_OK:
+        raise FAError(where, status)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_qkv(name, t, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4:
+        raise ValueError("%s must be a 4-D bf16 CUDA tensor [B,H,N,d]" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (
+            name, tuple(t.shape), tuple(shape)))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    load_library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_check_device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the status code."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return int(load_library().fa_check_device_status(_stream_handle(dev)))
+
+
+def fa_debug_expire_wait(device=None) -> None:
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    _check("fa_debug_expire_wait",
+           load_library().fa_debug_expire_wait(_stream_handle(dev)))
+
+
+def fa_bwd_set_phase_events(before_main=None, after_main=None) -> None:
+    """Have later fa_bwd calls record these torch.cuda.Event objects around
+    their main kernel (None, None turns it off)."""
+    def handle(ev):
+        if ev is None:
+            return None
+        return ctypes.c_void_p(ev.cuda_event)
+    load_library().fa_bwd_set_phase_events(handle(before_main),
+                                           handle(after_main))
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_fwd(q, k, v, causal: bool, scale: float, out=None, lse=None):
+    """Forward pass.  Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
+    lib = load_library()
+    _check_qkv("q", q)
+    _check_qkv("k", k, q.shape)
+    _check_qkv("v", v, q.shape)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_qkv("out", out, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    with torch.cuda.device(q.device):
+        _check("fa_fwd", lib.fa_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+            int(bool(causal)), float(scale), _stream_handle(q.device)))
+    return out, lse
+
+
+def fa_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None,
+           dk=None, dv=None, workspace=None):
+    """Backward pass.  Returns (dQ, dK, dV), bf16 [B,H,N,d] each."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    need = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=q.device)
+    with torch.cuda.device(q.device):
+        _check("fa_bwd", lib.fa_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), B, H, N, d,
+            int(bool(causal)), float(scale), _stream_handle(q.device)))
+    return dq, dk, dv
