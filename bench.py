@@ -225,6 +225,11 @@ def run_ours(args, w, rank, world, local):
     K = args.steps
     main_ev = [(torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # torch creates the CUDA event lazily and only times events it recorded
+    # itself: record each once here; the library re-records them later.
+    for a, b in main_ev:
+        a.record(stream)
+        b.record(stream)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None

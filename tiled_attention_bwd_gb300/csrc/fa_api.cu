@@ -24,7 +24,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxN = 65535 * fa::kTile;  // grid.y limit of the key-tile grid
+constexpr int kMaxN = 1 << 30;  // keeps every row index inside int
 
 struct DeviceCtx {
   bool ready = false;
@@ -96,6 +96,25 @@ fa_status make_tile_map(CUtensorMap* m, const void* base, int BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D view [BH][N][d] of the fp32 dQ accumulator; box = 128 rows x 32
+// columns (128 bytes), 128-byte swizzle.  Reduce-adds clip rows past N.
+fa_status make_acc_map(CUtensorMap* m, const void* base, int BH, int N,
+                       int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  fa_status s = encode_fn(&fn);
+  if (s != FA_OK) return s;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -111,11 +130,24 @@ fa_status check_shape(int B, int H, int N, int d, int causal, float scale,
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H > INT_MAX) return FA_ERR_UNSUPPORTED;
   if (N > kMaxN) return FA_ERR_UNSUPPORTED;
+  // One block per (head, 128-row tile) must fit a 31-bit grid.
+  if ((long long)B * H * ((N + fa::kTile - 1) / fa::kTile) > INT_MAX)
+    return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) *empty = true;
   return FA_OK;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Heads per scheduling group: as many heads as keep `bytes_per_head` of
+// re-read data within an L2 budget, at least one.
+int heads_per_group(int BH, size_t bytes_per_head) {
+  constexpr size_t kL2Budget = 32u << 20;
+  size_t g = bytes_per_head ? kL2Budget / bytes_per_head : (size_t)BH;
+  if (g < 1) g = 1;
+  if (g > (size_t)BH) g = (size_t)BH;
+  return (int)g;
+}
 
 struct WsLayout {
   size_t dq_acc_off, ddot_off, lse2_off, total;
@@ -172,7 +204,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
+  a.BH = BH;
   a.N = N;
+  // Re-read per head: its K and V.
+  a.group = heads_per_group(BH, (size_t)4 * N * d);
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = g_timeout_ns.load();
@@ -206,12 +241,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
   DeviceCtx* ctx = nullptr;
   if ((s = device_ctx(&ctx)) != FA_OK) return s;
   const int BH = B * H;
-  CUtensorMap tq, tk, tv, tdo;
+  char* ws = static_cast<char*>(workspace);
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tk, k, BH, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tdo, dout, BH, N, d)) != FA_OK) return s;
-  char* ws = static_cast<char*>(workspace);
+  if ((s = make_acc_map(&tdq, ws + w.dq_acc_off, BH, N, d)) != FA_OK) return s;
   fa::BwdArgs a{};
   a.o = static_cast<const __nv_bfloat16*>(o);
   a.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -225,6 +261,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
   a.BH = BH;
   a.N = N;
   a.N_pad = (int)align_up((size_t)N, fa::kTile);
+  // Re-read per head: Q and dO (bf16) and the fp32 dQ accumulator.
+  a.group = heads_per_group(BH, (size_t)8 * N * d);
   a.scale = scale;
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
@@ -235,7 +273,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
   if (e == cudaSuccess && g_ev_before_main)
     e = cudaEventRecord(g_ev_before_main, st);
   if (e == cudaSuccess)
-    e = fa::launch_bwd_main(tq, tk, tv, tdo, a, d, causal != 0, st);
+    e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, a, d, causal != 0, st);
   if (e == cudaSuccess && g_ev_after_main)
     e = cudaEventRecord(g_ev_after_main, st);
   if (e == cudaSuccess) e = fa::launch_bwd_post(a, d, elem_blocks, st);

@@ -16,13 +16,14 @@
 //         two-stage TMA ring (causal: only i >= j).  Per Q tile, five tcgen05
 //         MMAs: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P^T from TMEM),
 //         dK += dS^T Q and dQ_i = dS K (dS from smem, read K-major for the
-//         first and MN-major for the second).  dQ_i leaves TMEM as fp32
-//         atomic adds into the accumulator.
+//         first and MN-major for the second).  dQ_i leaves TMEM and is
+//         added into the fp32 accumulator by TMA reduce-add.
 //   post  dQ = scale * accumulator, rounded to bf16.
 //
 // Warps of the main kernel:
 //   0-3  thread = key row: P^T = exp2(S^T c - LSE2), then dS^T = P^T (dP^T - D)
-//   4-7  thread = query row: drain dQ_i from TMEM into global fp32 adds
+//   4-7  thread = query row: drain dQ_i from TMEM, stage it through the dS
+//        tile and add it into the fp32 accumulator with TMA reduce-add
 //   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
 // TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T and then dQ [128,256)
 // dK [256, 256+d)  dV [256+d, 256+2d).
@@ -66,6 +67,8 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t ds_free;
+  uint64_t red_ready;
+  uint64_t red_free;
   uint64_t acc_done;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -86,6 +89,8 @@ enum : uint32_t {
   kWBwdCmpAcc = 0x315,
   kWBwdDqFull = 0x411,
   kWBwdDqAcc = 0x412,
+  kWBwdDqRedFree = 0x413,
+  kWBwdDqRedReady = 0x414,
   kWBwdMisaligned = 0x5A1,
 };
 
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq,
                     const BwdArgs a) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -102,9 +108,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto* bars = reinterpret_cast<BwdBars*>(smem + L::kBarOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int j = blockIdx.y;                       // key tile
+  // Blocks resident together share a few heads, so their Q/dO tiles and dQ
+  // accumulator rows stay in L2; causal key tile 0 (the most query tiles)
+  // of each head starts first.
   const int n_tiles = (a.N + kTile - 1) / kTile;
+  const TileSlot slot = grouped_slot((int)blockIdx.x, n_tiles, a.BH, a.group);
+  const int bh = slot.bh;
+  const int j = slot.tile;                        // key tile
   const int i_begin = CAUSAL ? j : 0;             // first query tile
   const int nq = n_tiles - i_begin;
 
@@ -128,6 +138,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->red_ready, 128);
+    mbar_init(&bars->red_free, 1);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_done, 1);
     fence_mbar_init();
@@ -153,6 +165,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
+      prefetch_tmap(&tm_dq);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTileBytes);
 #pragma unroll
       for (int sb = 0; sb < L::kSub; ++sb) {
@@ -203,17 +216,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t ds_a = smem_addr(ds_s);
       const uint32_t tS = tmem, tDP = tmem + 128;
       const uint32_t tDK = tmem + 256, tDV = tmem + 256 + D;
-      bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
-      for (int it = 0; it < nq && ok; ++it) {
-        const int stage = it & 1;
-        const uint32_t sp = (uint32_t)((it >> 1) & 1);
-        const uint32_t par = (uint32_t)(it & 1);
-        ok = wait_bar(&bars->st_full[stage], sp, wc, kWBwdMmaSt);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t q_a = smem_addr(smem + L::kStageOff + stage * L::kStageBytes);
-        const uint32_t do_a = q_a + L::kTileBytes;
-        // S^T = K_j Q_i^T   [keys x queries], K = d
+      // Software pipeline: S^T and dP^T of tile it+1 are issued around the
+      // dK/dQ MMAs of tile it, so the P/dS warps work on tile it+1 while the
+      // tensor core finishes tile it.  Per iteration the issue order is
+      //   dV(it)  S^T(it+1)  dK(it)  dQ(it)  dP^T(it+1)
+      // S^T(it+1) may overwrite P^T(it) because dV(it) precedes it in the
+      // tensor core's in-order queue.
+      auto issue_st = [&](int it) {
+        const uint32_t q_a =
+            smem_addr(smem + L::kStageOff + (it & 1) * L::kStageBytes);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
@@ -221,13 +232,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  sdesc_sw128(q_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full);
-        if (it > 0) {
-          // dQ_{i-1} sits in the dP columns until drained.
-          ok = wait_bar(&bars->dq_free, par ^ 1u, wc, kWBwdMmaDqFree);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // dP^T = V_j dO_i^T   [keys x queries], K = d
+      };
+      auto issue_dp = [&](int it) {
+        const uint32_t do_a =
+            smem_addr(smem + L::kStageOff + (it & 1) * L::kStageBytes) +
+            L::kTileBytes;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
@@ -235,6 +244,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  sdesc_sw128(do_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
+      };
+      bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
+      if (ok) ok = wait_bar(&bars->st_full[0], 0, wc, kWBwdMmaSt);
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);   // S^T = K_j Q_i^T   [keys x queries], K = d
+        issue_dp(0);   // dP^T = V_j dO_i^T [keys x queries], K = d
+      }
+      for (int it = 0; it < nq && ok; ++it) {
+        const int stage = it & 1;
+        const uint32_t par = (uint32_t)(it & 1);
+        const uint32_t q_a = smem_addr(smem + L::kStageOff + stage * L::kStageBytes);
+        const uint32_t do_a = q_a + L::kTileBytes;
         ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
         if (!ok) break;
         tc_fence_after();
@@ -244,6 +266,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(tDV, tS + s * 8,
                  sdesc_sw128(do_a + s * 2048, kSubTileBytes, 1024), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
+        if (it + 1 < nq) {
+          ok = wait_bar(&bars->st_full[stage ^ 1], (uint32_t)(((it + 1) >> 1) & 1),
+                        wc, kWBwdMmaSt);
+          if (!ok) break;
+          tc_fence_after();
+          issue_st(it + 1);
+        }
         ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
         if (!ok) break;
         tc_fence_after();
@@ -261,9 +290,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(tDP, sdesc_sw128(ds_a + s * 2048, kSubTileBytes, 1024),
                  sdesc_sw128(k_a + s * 2048, kSubTileBytes, 1024), id_q,
                  s > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
+        mma_commit(&bars->dq_full);   // also: dS no longer read by MMAs
         mma_commit(&bars->st_empty[stage]);
-        mma_commit(&bars->ds_free);
+        if (it + 1 < nq) {
+          // dQ_it occupies the dP columns until the drain warps have read it.
+          ok = wait_bar(&bars->dq_free, par, wc, kWBwdMmaDqFree);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
       }
       if (ok) mma_commit(&bars->acc_done);
       mma_commit(&bars->mma_done);
@@ -289,36 +324,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[128];
-      tmem_ld32(tl + 0, s);
-      tmem_ld32(tl + 32, s + 32);
-      tmem_ld32(tl + 64, s + 64);
-      tmem_ld32(tl + 96, s + 96);
-      tmem_wait_ld();
-      reg_fence32(s);
-      reg_fence32(s + 32);
-      reg_fence32(s + 64);
-      reg_fence32(s + 96);
+      // P^T = exp2(S^T c - LSE2), in two halves of 64 queries so that only
+      // half a row of S is live; P half h goes to TMEM columns [32h, 32h+32),
+      // over S columns that have already been read.
       uint32_t pk[64];
       const bool diag = CAUSAL && (i == j);
 #pragma unroll
-      for (int e = 0; e < 128; e += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + e);
-        float x0 = fmaf(__uint_as_float(s[e + 0]), c, -l4.x);
-        float x1 = fmaf(__uint_as_float(s[e + 1]), c, -l4.y);
-        float x2 = fmaf(__uint_as_float(s[e + 2]), c, -l4.z);
-        float x3 = fmaf(__uint_as_float(s[e + 3]), c, -l4.w);
-        if (diag) {  // query e < key r is masked
-          if (e + 0 < r) x0 = -INFINITY;
-          if (e + 1 < r) x1 = -INFINITY;
-          if (e + 2 < r) x2 = -INFINITY;
-          if (e + 3 < r) x3 = -INFINITY;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t s[64];
+        tmem_ld32(tl + 64 * h, s);
+        tmem_ld32(tl + 64 * h + 32, s + 32);
+        tmem_wait_ld();
+        reg_fence32(s);
+        reg_fence32(s + 32);
+#pragma unroll
+        for (int e = 0; e < 64; e += 4) {
+          const int q = 64 * h + e;
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+          float x0 = fmaf(__uint_as_float(s[e + 0]), c, -l4.x);
+          float x1 = fmaf(__uint_as_float(s[e + 1]), c, -l4.y);
+          float x2 = fmaf(__uint_as_float(s[e + 2]), c, -l4.z);
+          float x3 = fmaf(__uint_as_float(s[e + 3]), c, -l4.w);
+          if (diag) {  // query q < key r is masked
+            if (q + 0 < r) x0 = -INFINITY;
+            if (q + 1 < r) x1 = -INFINITY;
+            if (q + 2 < r) x2 = -INFINITY;
+            if (q + 3 < r) x3 = -INFINITY;
+          }
+          pk[q / 2] = pack_bf16(ex2(x0), ex2(x1));
+          pk[q / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
         }
-        pk[e / 2] = pack_bf16(ex2(x0), ex2(x1));
-        pk[e / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
+        tmem_st32(tl + 32 * h, pk + 32 * h);
       }
-      tmem_st32(tl + 0, pk);
-      tmem_st32(tl + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
@@ -389,9 +426,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
+    // dQ_i leaves TMEM into registers (then the columns are released), is
+    // staged through the dS smem tile -- idle from the end of the dK/dQ MMAs
+    // until the P/dS warps write the next dS -- as [128 rows][32 fp32] boxes in
+    // the 128-byte swizzle layout, and is added into the fp32 accumulator by
+    // TMA reduce-add (whole 128-byte lines at L2).  D/32 boxes, in rounds of
+    // two (32 KB, the dS tile).
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const bool elected = (warp == 4 && lane == 0);
+    constexpr int kBoxes = D / 32;                  // 16 KB each
+    constexpr int kRounds = (kBoxes + 1) / 2;
+    int round_no = 0;                               // global count of rounds
     bool ok = run;
     for (int it = 0; it < nq && ok; ++it) {
       const int i = i_begin + it;
@@ -406,17 +453,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int ch = 0; ch < D / 32; ++ch) reg_fence32(acc + ch * 32);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
-      const int q = i * kTile + r;
-      if (q < a.N) {
-        float4* dst = reinterpret_cast<float4*>(a.dq_acc + ((size_t)bh * a.N + q) * D);
 #pragma unroll
-        for (int v4 = 0; v4 < D / 4; ++v4)
-          atomicAdd(dst + v4, make_float4(__uint_as_float(acc[4 * v4]),
-                                          __uint_as_float(acc[4 * v4 + 1]),
-                                          __uint_as_float(acc[4 * v4 + 2]),
-                                          __uint_as_float(acc[4 * v4 + 3])));
+      for (int rd = 0; rd < kRounds; ++rd, ++round_no) {
+        if (round_no > 0) {
+          // The previous round's boxes must have been read out by the TMA.
+          ok = wait_bar_warp(&bars->red_free, (uint32_t)((round_no - 1) & 1), wc,
+                             kWBwdDqRedFree);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int box = 2 * rd + b;
+          if (box >= kBoxes) break;
+          uint8_t* dst = ds_s + b * (kTile * 128) + r * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) * 16)) =
+                make_uint4(acc[32 * box + 4 * k], acc[32 * box + 4 * k + 1],
+                           acc[32 * box + 4 * k + 2], acc[32 * box + 4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->red_ready);
+        if (elected) {
+          ok = wait_bar(&bars->red_ready, (uint32_t)(round_no & 1), wc, kWBwdDqRedReady);
+          if (ok) {
+            for (int b = 0; b < 2 && 2 * rd + b < kBoxes; ++b)
+              tma_reduce_add_3d(&tm_dq, ds_s + b * (kTile * 128),
+                                (2 * rd + b) * 32, i * kTile, bh);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bars->red_free);
+          if (rd == kRounds - 1) mbar_arrive(&bars->ds_free);  // dS tile free
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
       }
     }
+    if (elected) bulk_wait_all();  // accumulator adds complete before exit
     // dV epilogue (rows = keys)
     if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdDqAcc);
     if (ok) {
@@ -515,15 +589,16 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
 template <int D, bool CAUSAL>
 cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
-                          const BwdArgs& a, cudaStream_t stream) {
+                          const CUtensorMap& tdq, const BwdArgs& a,
+                          cudaStream_t stream) {
   using L = BwdLayout<D>;
   auto kern = bwd_main_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  dim3 grid((unsigned)a.BH, (unsigned)n_tiles);
-  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  dim3 grid((unsigned)(a.BH * n_tiles));
+  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -540,13 +615,13 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
 
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const BwdArgs& a, int d, bool causal,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tdq, const BwdArgs& a, int d,
+                            bool causal, cudaStream_t stream) {
   if (d == 128)
-    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, a, stream)
-                  : launch_main_t<128, false>(tq, tk, tv, tdo, a, stream);
-  return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, a, stream)
-                : launch_main_t<64, false>(tq, tk, tv, tdo, a, stream);
+    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdq, a, stream)
+                  : launch_main_t<128, false>(tq, tk, tv, tdo, tdq, a, stream);
+  return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdq, a, stream)
+                : launch_main_t<64, false>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,

@@ -96,6 +96,26 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Block scheduling.  Heads are taken in groups of `group` heads, sized on
+// the host so one group's K/V (forward) or Q/dO/dQ rows (backward) fit in L2.
+// Within a group the tile index is slow and the head fast, so the blocks
+// that are resident together share few heads, and (with tile 0 the
+// heaviest) the longest blocks of a group start first.
+struct TileSlot {
+  int bh;
+  int tile;
+};
+__device__ __forceinline__ TileSlot grouped_slot(int linear, int n_tiles,
+                                                 int BH, int group) {
+  const int per_group = group * n_tiles;
+  const int g = linear / per_group;
+  const int r = linear - g * per_group;
+  const int rest = BH - g * group;
+  const int heads = rest < group ? rest : group;
+  const int t = r / heads;
+  return TileSlot{g * group + (r - t * heads), t};
+}
+
 // Aligns the dynamic shared memory base to 1024 bytes (128-byte swizzle atoms).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   uintptr_t a = reinterpret_cast<uintptr_t>(p);

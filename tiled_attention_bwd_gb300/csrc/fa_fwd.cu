@@ -103,11 +103,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto* bars = reinterpret_cast<FwdBars<S>*>(smem + L::kBarOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int n_pairs = (n_tiles + 1) / 2;
-  // Causal: heaviest (last) pairs are launched first.
-  const int pair = CAUSAL ? (n_pairs - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+  const TileSlot slot = grouped_slot((int)blockIdx.x, n_pairs, a.BH, a.group);
+  const int bh = slot.bh;
+  // Causal: the heaviest (last) pair of each head is scheduled first.
+  const int pair = CAUSAL ? (n_pairs - 1 - slot.tile) : slot.tile;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const int nkv0 = CAUSAL ? qt0 + 1 : n_tiles;
   const int nkv1 = (qt1 < n_tiles) ? (CAUSAL ? qt1 + 1 : n_tiles) : 0;
@@ -402,7 +403,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int n_pairs = (n_tiles + 1) / 2;
-  dim3 grid((unsigned)BH, (unsigned)n_pairs);
+  dim3 grid((unsigned)(BH * n_pairs));
   kern<<<grid, kFwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

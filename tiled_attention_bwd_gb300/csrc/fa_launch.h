@@ -13,7 +13,9 @@ struct DevState;
 struct FwdArgs {
   __nv_bfloat16* o;     // [BH, N, d]
   float* lse;           // [BH, N]
+  int BH;
   int N;
+  int group;            // heads per scheduling group
   float scale_log2;     // scale * log2(e): scores enter exp2 directly
   DevState* st;
   uint64_t timeout_ns;
@@ -32,6 +34,7 @@ struct BwdArgs {
   int BH;
   int N;
   int N_pad;                  // N rounded up to a multiple of 128
+  int group;                  // heads per scheduling group
   float scale;
   float scale_log2;
   DevState* st;
@@ -46,8 +49,8 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
                            cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const BwdArgs& a, int d, bool causal,
-                            cudaStream_t stream);
+                            const CUtensorMap& tdq, const BwdArgs& a, int d,
+                            bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
                             cudaStream_t stream);
 cudaError_t launch_expire_wait(DevState* st, uint64_t timeout_ns,
