@@ -12,8 +12,8 @@
 //   pre   D_i and LSE_i*log2(e) per row (padded to whole tiles: D = 0 and
 //         LSE2 = +inf past N, which zeroes P there); dQ accumulator := 0.
 //   main  one thread block per (batch, head, 128-key tile j).  K_j, V_j stay
-//         in smem; dK_j, dV_j accumulate in TMEM; Q_i, dO_i stream through a
-//         two-stage TMA ring (causal: only i >= j).  Per Q tile, five tcgen05
+//         in smem; dK_j, dV_j accumulate in TMEM; Q_i (two stages) and dO_i
+//         (one buffer) stream in by TMA (causal: only i >= j).  Per Q tile, five tcgen05
 //         MMAs: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P^T from TMEM),
 //         dK += dS^T Q and dQ_i = dS K (dS from smem, read K-major for the
 //         first and MN-major for the second).  dQ_i leaves TMEM and is
@@ -22,8 +22,9 @@
 //
 // Warps of the main kernel:
 //   0-3  thread = key row: P^T = exp2(S^T c - LSE2), then dS^T = P^T (dP^T - D)
-//   4-7  thread = query row: drain dQ_i from TMEM, stage it through the dS
-//        tile and add it into the fp32 accumulator with TMA reduce-add
+//   4-7  thread = query row: drain dQ_i from TMEM, stage it box by box
+//        through two 16 KB buffers and add it into the fp32 accumulator with
+//        TMA reduce-add
 //   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
 // TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T and then dQ [128,256)
 // dK [256, 256+d)  dV [256+d, 256+2d).
@@ -41,15 +42,20 @@ template <int D>
 struct BwdLayout {
   static constexpr int kSub = D / 64;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
-  static constexpr int kStageOff = 2 * kTileBytes;
-  // Q_i, dO_i, LSE2_i[128], D_i[128]
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kTile * 4;
-  static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
+  // Two Q stages, each Q_i followed by LSE2_i[128] and D_i[128] (fp32).
+  static constexpr int kQOff = 2 * kTileBytes;
+  static constexpr int kQStageBytes = kTileBytes + 2 * kTile * 4;
+  // One dO buffer: dO_i is free once dV_i is done and dO_{i+1} is first
+  // needed one dK/dQ pair later.
+  static constexpr int kDOOff = kQOff + 2 * kQStageBytes;
+  static constexpr int kDSOff = kDOOff + kTileBytes;
   static constexpr int kDSBytes = kTile * kTile * 2;  // 2 sub-tiles [128][64]
-  static constexpr int kBarOff = kDSOff + kDSBytes;
+  // dQ staging: two [128 rows][32 fp32] boxes of 16 KB, used alternately.
+  static constexpr int kStgOff = kDSOff + kDSBytes;
+  static constexpr int kStgBoxBytes = kTile * 128;
+  static constexpr int kBarOff = kStgOff + 2 * kStgBoxBytes;
   // d = 128 uses 231,680 of the 232,448 bytes a block may have, so the base
   // is taken as is (checked at run time); d = 64 keeps alignment slack.
   static constexpr int kSlack = (D == 128) ? 0 : 1024;
@@ -58,8 +64,10 @@ struct BwdLayout {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t st_full[2];
-  uint64_t st_empty[2];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t do_full;
+  uint64_t do_empty;
   uint64_t s_full;
   uint64_t dp_full;
   uint64_t p_full;
@@ -67,8 +75,8 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t ds_free;
-  uint64_t red_ready;
-  uint64_t red_free;
+  uint64_t stg_ready[2];
+  uint64_t stg_free[2];
   uint64_t acc_done;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -76,21 +84,23 @@ struct BwdBars {
 };
 
 enum : uint32_t {
-  kWBwdProdEmpty = 0x111,
+  kWBwdProdQEmpty = 0x111,
+  kWBwdProdDoEmpty = 0x112,
   kWBwdMmaKV = 0x211,
-  kWBwdMmaSt = 0x212,
+  kWBwdMmaQ = 0x212,
   kWBwdMmaDqFree = 0x213,
   kWBwdMmaP = 0x214,
   kWBwdMmaDs = 0x215,
-  kWBwdCmpSt = 0x311,
+  kWBwdMmaDo = 0x216,
+  kWBwdCmpQ = 0x311,
   kWBwdCmpS = 0x312,
   kWBwdCmpDp = 0x313,
   kWBwdCmpDsFree = 0x314,
   kWBwdCmpAcc = 0x315,
   kWBwdDqFull = 0x411,
   kWBwdDqAcc = 0x412,
-  kWBwdDqRedFree = 0x413,
-  kWBwdDqRedReady = 0x414,
+  kWBwdDqStgFree = 0x413,
+  kWBwdDqStgReady = 0x414,
   kWBwdMisaligned = 0x5A1,
 };
 
@@ -128,18 +138,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bars->abort = stop;
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->st_full[s], 1);
-      mbar_init(&bars->st_empty[s], 1);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->stg_ready[s], 4);  // one arrival per drain warp
+      mbar_init(&bars->stg_free[s], 1);
     }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->p_full, 4);    // one arrival per warp
+    mbar_init(&bars->ds_full, 4);   // one arrival per warp
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->dq_free, 4);   // one arrival per warp
     mbar_init(&bars->ds_free, 1);
-    mbar_init(&bars->red_ready, 128);
-    mbar_init(&bars->red_free, 1);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_done, 1);
     fence_mbar_init();
@@ -156,7 +168,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl wc{a.st, &bars->abort, a.timeout_ns};
   uint8_t* const k_s = smem + L::kKOff;
   uint8_t* const v_s = smem + L::kVOff;
+  uint8_t* const do_s = smem + L::kDOOff;
   uint8_t* const ds_s = smem + L::kDSOff;
+  uint8_t* const stg_s = smem + L::kStgOff;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
@@ -174,36 +188,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(v_s + sb * kSubTileBytes, &tm_v, &bars->kv_full, sb * 64,
                     j * kTile, bh);
       }
-      int last_par[2] = {-1, -1};
+      int q_par[2] = {-1, -1}, do_par = -1;
       bool ok = true;
       for (int it = 0; it < nq; ++it) {
         const int i = i_begin + it;
         const int stage = it & 1;
         const uint32_t sp = (uint32_t)((it >> 1) & 1);
-        ok = wait_bar(&bars->st_empty[stage], sp ^ 1u, wc, kWBwdProdEmpty);
+        // Q_i, LSE2_i, D_i into Q stage it%2
+        ok = wait_bar(&bars->q_empty[stage], sp ^ 1u, wc, kWBwdProdQEmpty);
         if (!ok) break;
-        uint8_t* st = smem + L::kStageOff + stage * L::kStageBytes;
-        mbar_arrive_expect_tx(&bars->st_full[stage],
-                              2 * L::kTileBytes + 2 * kTile * 4);
+        uint8_t* qs = smem + L::kQOff + stage * L::kQStageBytes;
+        mbar_arrive_expect_tx(&bars->q_full[stage], L::kTileBytes + 2 * kTile * 4);
 #pragma unroll
-        for (int sb = 0; sb < L::kSub; ++sb) {
-          tma_load_3d(st + sb * kSubTileBytes, &tm_q, &bars->st_full[stage],
+        for (int sb = 0; sb < L::kSub; ++sb)
+          tma_load_3d(qs + sb * kSubTileBytes, &tm_q, &bars->q_full[stage],
                       sb * 64, i * kTile, bh);
-          tma_load_3d(st + L::kTileBytes + sb * kSubTileBytes, &tm_do,
-                      &bars->st_full[stage], sb * 64, i * kTile, bh);
-        }
         const size_t row0 = (size_t)bh * a.N_pad + (size_t)i * kTile;
-        bulk_load(st + 2 * L::kTileBytes, a.lse2 + row0, kTile * 4,
-                  &bars->st_full[stage]);
-        bulk_load(st + 2 * L::kTileBytes + kTile * 4, a.ddot + row0, kTile * 4,
-                  &bars->st_full[stage]);
-        last_par[stage] = (int)sp;
+        bulk_load(qs + L::kTileBytes, a.lse2 + row0, kTile * 4, &bars->q_full[stage]);
+        bulk_load(qs + L::kTileBytes + kTile * 4, a.ddot + row0, kTile * 4,
+                  &bars->q_full[stage]);
+        q_par[stage] = (int)sp;
+        // dO_i into the single dO buffer
+        ok = wait_bar(&bars->do_empty, (uint32_t)(it & 1) ^ 1u, wc, kWBwdProdDoEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->do_full, L::kTileBytes);
+#pragma unroll
+        for (int sb = 0; sb < L::kSub; ++sb)
+          tma_load_3d(do_s + sb * kSubTileBytes, &tm_do, &bars->do_full,
+                      sb * 64, i * kTile, bh);
+        do_par = it & 1;
       }
       if (!ok) {
         drain_bar(&bars->kv_full, 0, a.timeout_ns);
         for (int s = 0; s < 2; ++s)
-          if (last_par[s] >= 0)
-            drain_bar(&bars->st_full[s], (uint32_t)last_par[s], a.timeout_ns);
+          if (q_par[s] >= 0)
+            drain_bar(&bars->q_full[s], (uint32_t)q_par[s], a.timeout_ns);
+        if (do_par >= 0) drain_bar(&bars->do_full, (uint32_t)do_par, a.timeout_ns);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -213,18 +233,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, D, true, true);
       const uint32_t k_a = smem_addr(k_s), v_a = smem_addr(v_s);
-      const uint32_t ds_a = smem_addr(ds_s);
+      const uint32_t do_a = smem_addr(do_s), ds_a = smem_addr(ds_s);
       const uint32_t tS = tmem, tDP = tmem + 128;
       const uint32_t tDK = tmem + 256, tDV = tmem + 256 + D;
+      auto q_addr = [&](int it) {
+        return smem_addr(smem + L::kQOff + (it & 1) * L::kQStageBytes);
+      };
       // Software pipeline: S^T and dP^T of tile it+1 are issued around the
       // dK/dQ MMAs of tile it, so the P/dS warps work on tile it+1 while the
       // tensor core finishes tile it.  Per iteration the issue order is
       //   dV(it)  S^T(it+1)  dK(it)  dQ(it)  dP^T(it+1)
       // S^T(it+1) may overwrite P^T(it) because dV(it) precedes it in the
       // tensor core's in-order queue.
-      auto issue_st = [&](int it) {
-        const uint32_t q_a =
-            smem_addr(smem + L::kStageOff + (it & 1) * L::kStageBytes);
+      auto issue_st = [&](int it) {  // S^T = K_j Q_i^T  [keys x queries]
+        const uint32_t q_a = q_addr(it);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
@@ -233,10 +255,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(&bars->s_full);
       };
-      auto issue_dp = [&](int it) {
-        const uint32_t do_a =
-            smem_addr(smem + L::kStageOff + (it & 1) * L::kStageBytes) +
-            L::kTileBytes;
+      auto issue_dp = [&]() {  // dP^T = V_j dO_i^T  [keys x queries]
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
@@ -246,17 +265,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(&bars->dp_full);
       };
       bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
-      if (ok) ok = wait_bar(&bars->st_full[0], 0, wc, kWBwdMmaSt);
+      if (ok) ok = wait_bar(&bars->q_full[0], 0, wc, kWBwdMmaQ);
       if (ok) {
         tc_fence_after();
-        issue_st(0);   // S^T = K_j Q_i^T   [keys x queries], K = d
-        issue_dp(0);   // dP^T = V_j dO_i^T [keys x queries], K = d
+        issue_st(0);
+        ok = wait_bar(&bars->do_full, 0, wc, kWBwdMmaDo);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp();
       }
       for (int it = 0; it < nq && ok; ++it) {
-        const int stage = it & 1;
         const uint32_t par = (uint32_t)(it & 1);
-        const uint32_t q_a = smem_addr(smem + L::kStageOff + stage * L::kStageBytes);
-        const uint32_t do_a = q_a + L::kTileBytes;
+        const uint32_t q_a = q_addr(it);
         ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
         if (!ok) break;
         tc_fence_after();
@@ -266,9 +287,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(tDV, tS + s * 8,
                  sdesc_sw128(do_a + s * 2048, kSubTileBytes, 1024), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bars->do_empty);   // dO_i no longer needed
         if (it + 1 < nq) {
-          ok = wait_bar(&bars->st_full[stage ^ 1], (uint32_t)(((it + 1) >> 1) & 1),
-                        wc, kWBwdMmaSt);
+          ok = wait_bar(&bars->q_full[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1),
+                        wc, kWBwdMmaQ);
           if (!ok) break;
           tc_fence_after();
           issue_st(it + 1);
@@ -284,20 +306,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                              1024),
                  sdesc_sw128(q_a + s * 2048, kSubTileBytes, 1024), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bars->q_empty[it & 1]);   // Q_i, LSE2_i, D_i released
         // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
 #pragma unroll
         for (int s = 0; s < kTile / 16; ++s)
           mma_ss(tDP, sdesc_sw128(ds_a + s * 2048, kSubTileBytes, 1024),
                  sdesc_sw128(k_a + s * 2048, kSubTileBytes, 1024), id_q,
                  s > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);   // also: dS no longer read by MMAs
-        mma_commit(&bars->st_empty[stage]);
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->ds_free);    // dS_i no longer read
         if (it + 1 < nq) {
           // dQ_it occupies the dP columns until the drain warps have read it.
           ok = wait_bar(&bars->dq_free, par, wc, kWBwdMmaDqFree);
+          if (ok) ok = wait_bar(&bars->do_full, par ^ 1u, wc, kWBwdMmaDo);
           if (!ok) break;
           tc_fence_after();
-          issue_dp(it + 1);
+          issue_dp();
         }
       }
       if (ok) mma_commit(&bars->acc_done);
@@ -316,10 +340,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int stage = it & 1;
       const uint32_t sp = (uint32_t)((it >> 1) & 1);
       const uint32_t par = (uint32_t)(it & 1);
-      ok = wait_bar_warp(&bars->st_full[stage], sp, wc, kWBwdCmpSt);
+      ok = wait_bar_warp(&bars->q_full[stage], sp, wc, kWBwdCmpQ);
       if (!ok) break;
       const float* lse2 = reinterpret_cast<const float*>(
-          smem + L::kStageOff + stage * L::kStageBytes + 2 * L::kTileBytes);
+          smem + L::kQOff + stage * L::kQStageBytes + L::kTileBytes);
       const float* dd = lse2 + kTile;
       ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
       if (!ok) break;
@@ -358,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      warp_arrive(&bars->p_full);
 
       ok = wait_bar_warp(&bars->dp_full, par, wc, kWBwdCmpDp);
       if (ok && it > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
@@ -395,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      warp_arrive(&bars->ds_full);
     }
     // dK epilogue (rows = keys)
     if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdCmpAcc);
@@ -426,19 +450,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
-    // dQ_i leaves TMEM into registers (then the columns are released), is
-    // staged through the dS smem tile -- idle from the end of the dK/dQ MMAs
-    // until the P/dS warps write the next dS -- as [128 rows][32 fp32] boxes in
-    // the 128-byte swizzle layout, and is added into the fp32 accumulator by
-    // TMA reduce-add (whole 128-byte lines at L2).  D/32 boxes, in rounds of
-    // two (32 KB, the dS tile).
+    // dQ_i leaves TMEM into registers (then the columns are released) and is
+    // added into the fp32 accumulator box by box ([128 rows][32 fp32] = 16 KB
+    // in the 128-byte swizzle layout) through two staging buffers used
+    // alternately, by TMA reduce-add (whole 128-byte lines at L2).  A buffer
+    // is rewritten only after the TMA has read the box before the last one.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const bool elected = (warp == 4 && lane == 0);
-    constexpr int kBoxes = D / 32;                  // 16 KB each
-    constexpr int kRounds = (kBoxes + 1) / 2;
-    int round_no = 0;                               // global count of rounds
+    constexpr int kBoxes = D / 32;
+    int g = 0;                                       // boxes staged so far
     bool ok = run;
     for (int it = 0; it < nq && ok; ++it) {
       const int i = i_begin + it;
@@ -452,39 +474,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) reg_fence32(acc + ch * 32);
       tc_fence_before();
-      mbar_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
+      warp_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
 #pragma unroll
-      for (int rd = 0; rd < kRounds; ++rd, ++round_no) {
-        if (round_no > 0) {
-          // The previous round's boxes must have been read out by the TMA.
-          ok = wait_bar_warp(&bars->red_free, (uint32_t)((round_no - 1) & 1), wc,
-                             kWBwdDqRedFree);
+      for (int b = 0; b < kBoxes; ++b, ++g) {
+        const int buf = g & 1;
+        if (g >= 2) {
+          ok = wait_bar_warp(&bars->stg_free[buf], (uint32_t)(((g >> 1) - 1) & 1),
+                             wc, kWBwdDqStgFree);
           if (!ok) break;
         }
+        uint8_t* dst = stg_s + buf * L::kStgBoxBytes + r * 128;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int box = 2 * rd + b;
-          if (box >= kBoxes) break;
-          uint8_t* dst = ds_s + b * (kTile * 128) + r * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) * 16)) =
-                make_uint4(acc[32 * box + 4 * k], acc[32 * box + 4 * k + 1],
-                           acc[32 * box + 4 * k + 2], acc[32 * box + 4 * k + 3]);
-        }
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) * 16)) =
+              make_uint4(acc[32 * b + 4 * k], acc[32 * b + 4 * k + 1],
+                         acc[32 * b + 4 * k + 2], acc[32 * b + 4 * k + 3]);
         fence_proxy_async_smem();
-        mbar_arrive(&bars->red_ready);
+        warp_arrive(&bars->stg_ready[buf]);
         if (elected) {
-          ok = wait_bar(&bars->red_ready, (uint32_t)(round_no & 1), wc, kWBwdDqRedReady);
+          ok = wait_bar(&bars->stg_ready[buf], (uint32_t)((g >> 1) & 1), wc,
+                        kWBwdDqStgReady);
           if (ok) {
-            for (int b = 0; b < 2 && 2 * rd + b < kBoxes; ++b)
-              tma_reduce_add_3d(&tm_dq, ds_s + b * (kTile * 128),
-                                (2 * rd + b) * 32, i * kTile, bh);
+            tma_reduce_add_3d(&tm_dq, stg_s + buf * L::kStgBoxBytes, b * 32,
+                              i * kTile, bh);
             bulk_commit_group();
-            bulk_wait_read_all();
           }
-          mbar_arrive(&bars->red_free);
-          if (rd == kRounds - 1) mbar_arrive(&bars->ds_free);  // dS tile free
+          if (b > 0) {
+            // The previous box (other buffer) has been read: release it.
+            bulk_wait_read_allbut1();
+            mbar_arrive(&bars->stg_free[buf ^ 1]);
+          }
+          if (b == kBoxes - 1) {
+            bulk_wait_read_all();
+            mbar_arrive(&bars->stg_free[buf]);
+          }
         }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;

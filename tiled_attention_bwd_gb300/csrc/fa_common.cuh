@@ -86,14 +86,23 @@ static __device__ __noinline__ bool drain_bar(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Warp-uniform wait: every lane waits, and the warp proceeds only if all
-// lanes saw the phase complete (so warp-collective tcgen05 loads/stores are
-// never executed by a partial warp).
+// Warp-uniform wait: every lane waits (a single polling lane with the rest
+// parked was measured markedly slower), and the warp proceeds only if all
+// lanes saw the phase complete, so warp-collective tcgen05 loads/stores are
+// never executed by a partial warp.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity,
                                               const WaitCtl& c,
                                               uint32_t where) {
   bool ok = wait_bar(bar, parity, c, where);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-collective arrive: the warp synchronises (ordering every lane's
+// earlier writes before lane 0's release) and lane 0 arrives once.  Barriers
+// fed this way count warps, not threads.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // Block scheduling.  Heads are taken in groups of `group` heads, sized on

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->q_full[t], 1);
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t], 4);   // one arrival per warp
       mbar_init(&bars->o_done[t], 1);
     }
     for (int s = 0; s < S; ++s) {
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st32(tS + 32, pk + 32);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[t]);
+        warp_arrive(&bars->p_full[t]);
       }
       if (ok) ok = wait_bar_warp(&bars->o_done[t], 0, wc, kWFwdSmO);
       if (ok) {
