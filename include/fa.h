@@ -137,6 +137,35 @@ fa_status fa_debug_expire_wait(void* stream);
  */
 void fa_bwd_set_phase_events(void* before_main, void* after_main);
 
+/*
+ * Backward pass for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this entry point exists for callers of this library.)
+ *
+ * Same arguments and results as fa_bwd, without the workspace: a plug-in
+ * that is handed only the tensors and owns no allocator, a serving or
+ * training loop that reserves all memory up front and forbids allocation on
+ * its hot path, or code that must not call cudaMalloc because it synchronises
+ * the device can still run the backward pass.  The scratch is a fixed
+ * 64 MiB array in device memory (fa_bwd_noalloc_max_workspace()), held by
+ * every GPU that loads the library until the process exits; neither the
+ * caller nor the library allocates anything per call.
+ *   - Shapes whose fa_bwd_workspace_size() exceeds that maximum are rejected
+ *     with FA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array, so calls whose kernels overlap on the
+ *     GPU (other streams, other host threads) race on it.  Its contents
+ *     from a previous call do not matter: each call rewrites what it reads.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         void* dq, void* dk, void* dv, int B, int H, int N,
+                         int d, int causal, float scale, void* stream);
+
+/* Size in bytes of the fixed scratch array used by fa_bwd_noalloc. */
+size_t fa_bwd_noalloc_max_workspace(void);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -313,6 +313,60 @@ fa_status fa_debug_expire_wait(void* stream) {
 }
 
 }  // extern "C"
+// ---------------------------------------------------------------------------
+// Backward pass without any device allocation by the caller or the library.
+//
+// Some callers cannot obtain device memory at the point where they run the
+// backward pass: code that owns no allocator (a plug-in handed only the
+// tensors), serving or training loops that reserve all memory up front and
+// forbid allocation on the hot path, and code that must not call cudaMalloc
+// because it synchronises the device.  For them the workspace lives in a
+// fixed array in device memory that every GPU which loads this library keeps
+// until the process exits.
+//
+// On the first call on a device (with that device current) the array's
+// device address is looked up once with cudaGetSymbolAddress; make that first
+// call before any stream capture.  All calls share the array: two calls whose
+// kernels overlap on the GPU (different streams, or other threads) race on
+// it.  Nothing in it needs to start at zero across calls: the pre kernel
+// rewrites every part the backward reads (D, LSE*log2e, and a zeroed dQ
+// accumulator) on every call.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+extern "C" size_t fa_bwd_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
+
+extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
+                                    const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk,
+                                    void* dv, int B, int H, int N, int d,
+                                    int causal, float scale, void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (ws_layout(B, H, N, d).total > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return FA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+        return FA_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch,
+                kNoAllocScratchBytes, B, H, N, d, causal, scale, stream);
+}
 
 namespace fa {
 

@@ -69,6 +69,11 @@ def open_library(path: str):
     lib.fa_debug_expire_wait.restype = i
     lib.fa_bwd_set_phase_events.argtypes = [vp, vp]
     lib.fa_bwd_set_phase_events.restype = None
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   i, i, i, i, i, f, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc_max_workspace.argtypes = []
+    lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     return lib
@@ -188,4 +193,29 @@ def fa_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None,
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
             workspace.numel() * workspace.element_size(), B, H, N, d,
             int(bool(causal)), float(scale), _stream_handle(q.device)))
+    return dq, dk, dv
+
+
+def fa_bwd_noalloc_max_workspace() -> int:
+    return int(load_library().fa_bwd_noalloc_max_workspace())
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, causal: bool, scale: float, dq,
+                   dk, dv):
+    """Backward pass through the entry point that allocates nothing: the
+    caller passes preallocated dq, dk, dv and the library uses its fixed
+    device scratch array instead of a workspace."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                    ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    with torch.cuda.device(q.device):
+        _check("fa_bwd_noalloc", lib.fa_bwd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
+            float(scale), _stream_handle(q.device)))
     return dq, dk, dv
