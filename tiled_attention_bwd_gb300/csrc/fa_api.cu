@@ -77,16 +77,16 @@ fa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return FA_OK;
 }
 
-// 3-D view [BH][N][d] of a bf16 [B,H,N,d] tensor; box = 128 rows x 64 columns
-// (128 bytes, the swizzle width).  Rows past N read as zeros.
+// 3-D view [BH][N][d] of a bf16 [B,H,N,d] tensor; box = `box_rows` rows x 64
+// columns (128 bytes, the swizzle width).  Rows past N read as zeros.
 fa_status make_tile_map(CUtensorMap* m, const void* base, int BH, int N,
-                        int d) {
+                        int d, int box_rows = fa::kTile) {
   PFN_cuTensorMapEncodeTiled_v12000 fn;
   fa_status s = encode_fn(&fn);
   if (s != FA_OK) return s;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr,
@@ -212,7 +212,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
   a.st = ctx->state;
   a.timeout_ns = g_timeout_ns.load();
   cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
-                                 static_cast<cudaStream_t>(stream));
+                                 ctx->sm_count, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -7,9 +7,9 @@
 // warp-specialised pipeline of "GPU Performance Optimization Batch 1 --
 // Design Spec", Item 3, sections "TMA" and "Warp Specialization").
 //
-// One thread block owns two 128-row Q tiles of one (batch, head) and streams
-// the 128-row K/V tiles past them:
-//   warp 8      TMA producer: Q0, Q1 once; K_j, V_j through a smem ring.
+// Persistent blocks (one per SM) take work items of two 128-row Q tiles of
+// one (batch, head) and stream the 128-row K/V tiles past them:
+//   warp 8      TMA producer: Q0, Q1 once per item; K_j, V_j through a ring.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //               O_t += P_t V_j with P_t read straight from TMEM.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1; thread = row.
@@ -20,8 +20,7 @@
 // tile's MMAs (ping-pong).  Causal blocks stop at the diagonal tile; only the
 // diagonal (and a ragged last tile) is masked.
 //
-// TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+d)
-// O1 [256+d, 256+2d).  P_t occupies the first 64 columns of S_t.
+// TMEM columns (512 allocated): S0, S1 | O0, O1 (see FwdLayout).
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -33,6 +32,16 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 
+// Shared memory: two Q tiles and a ring of K/V tiles, all 128 rows.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
+// P_t (bf16 pairs) is written over the first 64 columns of S_t.
+//
+// Measured on this part: a lone chain of M=128 tcgen05 MMAs with both
+// operands in smem runs at about 40% of peak, one with A in TMEM at full
+// rate, and the forward's interleaving of S = Q K^T (smem x smem) with
+// O += P V (TMEM x smem) runs at full rate; MMAs with N or K of 64 run well
+// below it.  Hence 128-key tiles, P kept in TMEM, and two Q tiles whose MMAs
+// interleave.
 template <int D>
 struct FwdLayout {
   static constexpr int kSub = D / 64;             // 64-column sub-tiles
@@ -47,6 +56,7 @@ struct FwdLayout {
 template <int STAGES>
 struct FwdBars {
   uint64_t q_full[2];
+  uint64_t q_empty[2];
   uint64_t kv_full[STAGES];
   uint64_t kv_empty[STAGES];
   uint64_t s_full[2];
@@ -60,6 +70,7 @@ struct FwdBars {
 // Where-codes of bounded waits (recorded when a wait expires).
 enum : uint32_t {
   kWFwdProdEmpty = 0x101,
+  kWFwdProdQ = 0x102,
   kWFwdMmaQ = 0x201,
   kWFwdMmaKV = 0x202,
   kWFwdMmaP = 0x203,
@@ -67,18 +78,21 @@ enum : uint32_t {
   kWFwdSmO = 0x302,
 };
 
+// S_t = Q_t K^T: M = N = 128, K = d; both operands K-major in smem.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr,
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr,
                                          uint32_t k_addr) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
     const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024),
+    mma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024),
            sdesc_sw128(k_addr + off, 16, 1024), id, s > 0 ? 1u : 0u);
   }
 }
 
+// O_t (+)= P_t V: M = 128, N = d, K = 128 keys; A = P from TMEM, B = V
+// read MN-major (d contiguous in smem).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
                                          uint32_t v_addr, bool accumulate) {
@@ -91,6 +105,42 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
   }
 }
 
+// One work item = (head, pair of Q tiles).  Causal: pair p needs key tiles
+// 0..2p (first Q tile) and 0..2p+1 (second); the second tile may not exist
+// when the tile count is odd.
+struct FwdItem {
+  int bh, qt0, qt1, nkv0, nkv1, nkv;
+};
+// Items are ordered heaviest first over the whole grid (pair index slow,
+// head fast; causal pairs from the last one down).  The forward re-reads
+// little, so global balance matters more here than L2 grouping by head.
+template <bool CAUSAL>
+__device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
+                                            int BH) {
+  const int rank = w / BH;
+  const int pair = CAUSAL ? (n_pairs - 1 - rank) : rank;
+  FwdItem it;
+  it.bh = w - rank * BH;
+  it.qt0 = 2 * pair;
+  it.qt1 = 2 * pair + 1;
+  it.nkv0 = CAUSAL ? it.qt0 + 1 : n_tiles;
+  it.nkv1 = (it.qt1 < n_tiles) ? (CAUSAL ? it.qt1 + 1 : n_tiles) : 0;
+  it.nkv = it.nkv0 > it.nkv1 ? it.nkv0 : it.nkv1;
+  return it;
+}
+
+// Item of block b in round r: rounds of gridDim.x items are dealt to the
+// blocks alternately forwards and backwards, so that with items sorted by
+// decreasing cost every block gets a similar total.
+__device__ __forceinline__ int fwd_round_item(int r) {
+  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+  return r * g + ((r & 1) ? (g - 1 - b) : b);
+}
+
+// Persistent: one block per SM walks its items round by round.  Barrier
+// phases run on across items, so the producer fetches the next item's Q and
+// K/V while the current one finishes, and the next item's first Q K^T
+// overlaps the softmax warps' epilogue.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -105,19 +155,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int n_pairs = (n_tiles + 1) / 2;
-  const TileSlot slot = grouped_slot((int)blockIdx.x, n_pairs, a.BH, a.group);
-  const int bh = slot.bh;
-  // Causal: the heaviest (last) pair of each head is scheduled first.
-  const int pair = CAUSAL ? (n_pairs - 1 - slot.tile) : slot.tile;
-  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
-  const int nkv0 = CAUSAL ? qt0 + 1 : n_tiles;
-  const int nkv1 = (qt1 < n_tiles) ? (CAUSAL ? qt1 + 1 : n_tiles) : 0;
-  const int nkv = nkv0 > nkv1 ? nkv0 : nkv1;
+  const int n_items = a.BH * n_pairs;
 
   if (threadIdx.x == 0) {
     bars->abort = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);   // one arrival per warp
       mbar_init(&bars->o_done[t], 1);
@@ -146,46 +190,54 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full[0], L::kTileBytes);
-#pragma unroll
-      for (int sb = 0; sb < L::kSub; ++sb)
-        tma_load_3d(smem + L::kQOff + sb * kSubTileBytes, &tm_q,
-                    &bars->q_full[0], sb * 64, qt0 * kTile, bh);
-      if (nkv1 > 0) {
-        mbar_arrive_expect_tx(&bars->q_full[1], L::kTileBytes);
-#pragma unroll
-        for (int sb = 0; sb < L::kSub; ++sb)
-          tma_load_3d(smem + L::kQOff + L::kTileBytes + sb * kSubTileBytes,
-                      &tm_q, &bars->q_full[1], sb * 64, qt1 * kTile, bh);
-      }
       int last_par[S];
 #pragma unroll
       for (int s = 0; s < S; ++s) last_par[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t q_cnt0 = 0, q_cnt1 = 0;   // loads issued into each Q buffer
       bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        for (int w = 0; w < 2; ++w) {  // 0: K_j, 1: V_j
-          ok = wait_bar(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
+      for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
+           w = fwd_round_item(++r)) {
+        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || (t == 1 && itm.nkv1 == 0)) break;
+          uint32_t& q_cnt = t ? q_cnt1 : q_cnt0;
+          // Q_t must no longer be read by the previous item's Q K^T.
+          ok = wait_bar(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->kv_full[stage], L::kTileBytes);
-          const CUtensorMap* m = w ? &tm_v : &tm_k;
+          mbar_arrive_expect_tx(&bars->q_full[t], L::kTileBytes);
 #pragma unroll
           for (int sb = 0; sb < L::kSub; ++sb)
-            tma_load_3d(smem + L::kKVOff + stage * L::kTileBytes +
-                            sb * kSubTileBytes,
-                        m, &bars->kv_full[stage], sb * 64, j * kTile, bh);
-          last_par[stage] = (int)phase;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
+            tma_load_3d(smem + L::kQOff + t * L::kTileBytes + sb * kSubTileBytes,
+                        &tm_q, &bars->q_full[t], sb * 64,
+                        (t ? itm.qt1 : itm.qt0) * kTile, itm.bh);
+          ++q_cnt;
+        }
+        for (int j = 0; j < itm.nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {  // 0: K_j, 1: V_j
+            ok = wait_bar(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->kv_full[stage], L::kTileBytes);
+            const CUtensorMap* m = kv ? &tm_v : &tm_k;
+#pragma unroll
+            for (int sb = 0; sb < L::kSub; ++sb)
+              tma_load_3d(smem + L::kKVOff + stage * L::kTileBytes +
+                              sb * kSubTileBytes,
+                          m, &bars->kv_full[stage], sb * 64, j * kTile, itm.bh);
+            last_par[stage] = (int)phase;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
       if (!ok) {
         // Stopping: let every copy this thread started land before exit.
-        drain_bar(&bars->q_full[0], 0, a.timeout_ns);
-        if (nkv1 > 0) drain_bar(&bars->q_full[1], 0, a.timeout_ns);
+        if (q_cnt0 > 0) drain_bar(&bars->q_full[0], (q_cnt0 - 1) & 1u, a.timeout_ns);
+        if (q_cnt1 > 0) drain_bar(&bars->q_full[1], (q_cnt1 - 1) & 1u, a.timeout_ns);
         for (int s = 0; s < S; ++s)
           if (last_par[s] >= 0)
             drain_bar(&bars->kv_full[s], (uint32_t)last_par[s], a.timeout_ns);
@@ -194,71 +246,88 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && run) {
-      const uint32_t q_addr0 = smem_addr(smem + L::kQOff);
-      const uint32_t q_addr1 = q_addr0 + L::kTileBytes;
+      // Per-tile addresses are computed, not indexed, so that nothing of
+      // this thread's state lives in local memory.
+      const uint32_t q_base = smem_addr(smem + L::kQOff);
       const uint32_t kv_addr = smem_addr(smem + L::kKVOff);
-      const uint32_t tS0 = tmem, tS1 = tmem + 128;
-      const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+      auto q_addr = [&](int t) { return q_base + (uint32_t)(t * L::kTileBytes); };
+      auto tS = [&](int t) { return tmem + (uint32_t)(t * 128); };
+      auto tO = [&](int t) { return tmem + (uint32_t)(256 + t * D); };
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = wait_bar(&bars->q_full[0], 0, wc, kWFwdMmaQ);
-      if (ok && nkv1 > 0) ok = wait_bar(&bars->q_full[1], 0, wc, kWFwdMmaQ);
-      // K_0
-      int k_stage = stage;
-      if (ok) ok = wait_bar(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
-      if (++stage == S) { stage = 0; phase ^= 1u; }
-      if (ok) {
-        tc_fence_after();
-        issue_qk<D>(tS0, q_addr0, kv_addr + k_stage * L::kTileBytes);
-        mma_commit(&bars->s_full[0]);
-        if (nkv1 > 0) {
-          issue_qk<D>(tS1, q_addr1, kv_addr + k_stage * L::kTileBytes);
-          mma_commit(&bars->s_full[1]);
+      uint32_t q_cnt0 = 0, q_cnt1 = 0, p_cnt0 = 0, p_cnt1 = 0;
+      bool ok = true;
+      auto next_kv = [&](int& st) -> bool {
+        st = stage;
+        const bool rr = wait_bar(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
         }
-        mma_commit(&bars->kv_empty[k_stage]);
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int v_stage = stage;
-        ok = wait_bar(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        return rr;
+      };
+      // Q K^T for tile t and key tile x; after the tile's last one, Q_t is
+      // released to the producer (in-order completion).
+      auto qk = [&](int t, int x, int nkv_t, uint32_t k_a) {
+        issue_qk<D>(tS(t), q_addr(t), k_a);
+        mma_commit(&bars->s_full[t]);
+        if (x == nkv_t - 1) mma_commit(&bars->q_empty[t]);
+      };
+      for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
+           w = fwd_round_item(++r)) {
+        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
+        ok = wait_bar(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
+        ++q_cnt0;
+        if (ok && itm.nkv1 > 0) {
+          ok = wait_bar(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
+          ++q_cnt1;
+        }
+        int k_stage = 0;
+        if (ok) ok = next_kv(k_stage);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t v_addr = kv_addr + v_stage * L::kTileBytes;
-        if (j < nkv0) {
-          ok = wait_bar(&bars->p_full[0], (uint32_t)(j & 1), wc, kWFwdMmaP);
+        qk(0, 0, itm.nkv0, kv_addr + k_stage * L::kTileBytes);
+        if (itm.nkv1 > 0) qk(1, 0, itm.nkv1, kv_addr + k_stage * L::kTileBytes);
+        mma_commit(&bars->kv_empty[k_stage]);
+        for (int j = 0; j < itm.nkv && ok; ++j) {
+          int v_stage = 0;
+          ok = next_kv(v_stage);
           if (!ok) break;
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, v_addr, j > 0);
+          const uint32_t v_addr = kv_addr + v_stage * L::kTileBytes;
+          int kn_stage = -1;
+          // Tile 0: P V for key tile j, then Q K^T for key tile j+1.
+          if (j < itm.nkv0) {
+            ok = wait_bar(&bars->p_full[0], p_cnt0 & 1u, wc, kWFwdMmaP);
+            ++p_cnt0;
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<D>(tO(0), tS(0), v_addr, j > 0);
+          }
+          if (j + 1 < itm.nkv) {
+            ok = next_kv(kn_stage);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          if (j + 1 < itm.nkv0)
+            qk(0, j + 1, itm.nkv0, kv_addr + kn_stage * L::kTileBytes);
+          else if (j == itm.nkv0 - 1)
+            mma_commit(&bars->o_done[0]);
+          // Tile 1: the same; V_j is released after both tiles used it.
+          if (j < itm.nkv1) {
+            ok = wait_bar(&bars->p_full[1], p_cnt1 & 1u, wc, kWFwdMmaP);
+            ++p_cnt1;
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<D>(tO(1), tS(1), v_addr, j > 0);
+          }
+          mma_commit(&bars->kv_empty[v_stage]);
+          if (j + 1 < itm.nkv1)
+            qk(1, j + 1, itm.nkv1, kv_addr + kn_stage * L::kTileBytes);
+          else if (j == itm.nkv1 - 1)
+            mma_commit(&bars->o_done[1]);
+          if (kn_stage >= 0) mma_commit(&bars->kv_empty[kn_stage]);
         }
-        int kn_stage = -1;
-        if (j + 1 < nkv) {
-          kn_stage = stage;
-          ok = wait_bar(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
-          if (++stage == S) { stage = 0; phase ^= 1u; }
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t kn_addr = kv_addr + (kn_stage < 0 ? 0 : kn_stage) * L::kTileBytes;
-        if (j + 1 < nkv0) {
-          issue_qk<D>(tS0, q_addr0, kn_addr);
-          mma_commit(&bars->s_full[0]);
-        } else if (j == nkv0 - 1) {
-          mma_commit(&bars->o_done[0]);
-        }
-        if (j < nkv1) {
-          ok = wait_bar(&bars->p_full[1], (uint32_t)(j & 1), wc, kWFwdMmaP);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv<D>(tO1, tS1, v_addr, j > 0);
-        }
-        mma_commit(&bars->kv_empty[v_stage]);
-        if (j + 1 < nkv1) {
-          issue_qk<D>(tS1, q_addr1, kn_addr);
-          mma_commit(&bars->s_full[1]);
-        } else if (j == nkv1 - 1) {
-          mma_commit(&bars->o_done[1]);
-        }
-        if (kn_stage >= 0) mma_commit(&bars->kv_empty[kn_stage]);
       }
       // Every MMA issued above must finish before TMEM is released.
       mma_commit(&bars->mma_done);
@@ -267,20 +336,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else {
     // ------------------------------------------------- softmax (thread = row)
     const int t = warp >> 2, quarter = warp & 3;
-    const int nkv_t = t ? nkv1 : nkv0;
-    if (run && nkv_t > 0) {
-      const int qrow = (2 * pair + t) * kTile + quarter * 32 + lane;
-      const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-      const uint32_t tS = tl + t * 128;
-      const uint32_t tO = tl + 256 + t * D;
-      const float c = a.scale_log2;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = tl + t * 128;
+    const uint32_t tO = tl + 256 + t * D;
+    const float c = a.scale_log2;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = run;
+    for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
+         w = fwd_round_item(++r)) {
+      const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
+      const int nkv_t = t ? itm.nkv1 : itm.nkv0;
+      if (nkv_t == 0) continue;
+      const int qrow = (t ? itm.qt1 : itm.qt0) * kTile + quarter * 32 + lane;
       float m_ref = -INFINITY, l = 0.f;
-      bool ok = true;
       for (int j = 0; j < nkv_t; ++j) {
-        if (!wait_bar_warp(&bars->s_full[t], (uint32_t)(j & 1), wc, kWFwdSmS)) {
-          ok = false;
-          break;
-        }
+        ok = wait_bar_warp(&bars->s_full[t], s_cnt & 1u, wc, kWFwdSmS);
+        ++s_cnt;
+        if (!ok) break;
         tc_fence_after();
         uint32_t s[128];
         tmem_ld32(tS + 0, s);
@@ -293,19 +365,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         reg_fence32(s + 64);
         reg_fence32(s + 96);
         // Mask: the diagonal tile (causal) or keys past N (ragged last tile).
-        const bool masked_tile = (j == nkv_t - 1) && (CAUSAL || (a.N & (kTile - 1)));
-        float mx = -INFINITY;
-        if (masked_tile) {
+        if ((j == nkv_t - 1) && (CAUSAL || (a.N & (kTile - 1)))) {
           const int lim = (CAUSAL ? qrow : a.N - 1) - j * kTile;
 #pragma unroll
-          for (int e = 0; e < 128; ++e) {
+          for (int e = 0; e < 128; ++e)
             if (e > lim) s[e] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(s[e]));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(s[e]));
         }
+        // Row max as eight independent chains (a single chain of 128
+        // dependent max operations dominated the softmax latency).
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(s[k]);
+#pragma unroll
+        for (int e = 8; e < 128; ++e)
+          mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(s[e]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_tile = mx * c;
         // Lazy rescale: keep the reference max until the row max exceeds it
         // by more than the threshold; exp2(x - m_ref) <= 2^8 meanwhile.
@@ -316,8 +391,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_ref = m_tile;
         }
         l *= alpha;
+        const float neg_m = -m_ref;
+        float l8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
+        // P is packed in place: pair (e, e+1) goes to s[e/2], a slot whose
+        // score has already been consumed, so no second array is live.
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[e + 0]), c, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), c, neg_m));
+          l8[e & 7] += p0;
+          l8[(e + 1) & 7] += p1;
+          s[e / 2] = pack_bf16(p0, p1);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        tmem_st32(tS + 0, s);
+        tmem_st32(tS + 32, s + 32);
         if (j > 0 && __any_sync(0xffffffffu, bump)) {
-          // O_t holds P V for tiles < j (the S_t(j) commit came after them).
+          // Rescale O_t, which holds P V for tiles < j (the S_t(j) commit
+          // came after them); done after P is stored so that the scores are
+          // no longer live.  P V for tile j waits for p_full below.
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
@@ -330,56 +424,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st32(tO + ch * 32, o);
           }
         }
-        const float neg_m = -m_ref;
-        uint32_t pk[64];
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 128; e += 4) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[e + 0]), c, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), c, neg_m));
-          const float p2 = ex2(fmaf(__uint_as_float(s[e + 2]), c, neg_m));
-          const float p3 = ex2(fmaf(__uint_as_float(s[e + 3]), c, neg_m));
-          l0 += p0;
-          l1 += p1;
-          l2 += p2;
-          l3 += p3;
-          pk[e / 2] = pack_bf16(p0, p1);
-          pk[e / 2 + 1] = pack_bf16(p2, p3);
-        }
-        l += (l0 + l1) + (l2 + l3);
-        tmem_st32(tS + 0, pk);
-        tmem_st32(tS + 32, pk + 32);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&bars->p_full[t]);
       }
-      if (ok) ok = wait_bar_warp(&bars->o_done[t], 0, wc, kWFwdSmO);
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = 1.0f / l;
-        const bool valid = qrow < a.N;
-        __nv_bfloat16* orow = a.o + ((size_t)bh * a.N + (valid ? qrow : 0)) * D;
+      if (!ok) break;
+      ok = wait_bar_warp(&bars->o_done[t], o_cnt & 1u, wc, kWFwdSmO);
+      ++o_cnt;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const bool valid = qrow < a.N;
+      __nv_bfloat16* orow = a.o + ((size_t)itm.bh * a.N + (valid ? qrow : 0)) * D;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-          uint32_t pk[16];
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(tO + ch * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
-                              __uint_as_float(o[2 * e + 1]) * inv_l);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
+                            __uint_as_float(o[2 * e + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                   pk[4 * v4 + 3]);
-          }
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                 pk[4 * v4 + 3]);
         }
-        if (valid) a.lse[(size_t)bh * a.N + qrow] = (m_ref + lg2(l)) * kLn2;
       }
+      if (valid) a.lse[(size_t)itm.bh * a.N + qrow] = (m_ref + lg2(l)) * kLn2;
+      // The next item's first P V (which overwrites O_t) is issued only after
+      // this warp group's next p_full arrival, so O_t is read out first.
+      tc_fence_before();
     }
   }
 
@@ -395,16 +474,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
-                         cudaStream_t stream) {
+                         int grid_blocks, cudaStream_t stream) {
   using L = FwdLayout<D>;
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int n_pairs = (n_tiles + 1) / 2;
-  dim3 grid((unsigned)(BH * n_pairs));
-  kern<<<grid, kFwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, a);
+  const int n_items = BH * ((n_tiles + 1) / 2);
+  const int blocks = n_items < grid_blocks ? n_items : grid_blocks;
+  kern<<<blocks, kFwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -412,12 +491,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                       bool causal, cudaStream_t stream) {
+                       bool causal, int grid_blocks, cudaStream_t stream) {
   if (d == 128)
-    return causal ? launch_fwd_t<128, true>(tq, tk, tv, a, BH, stream)
-                  : launch_fwd_t<128, false>(tq, tk, tv, a, BH, stream);
-  return causal ? launch_fwd_t<64, true>(tq, tk, tv, a, BH, stream)
-                : launch_fwd_t<64, false>(tq, tk, tv, a, BH, stream);
+    return causal ? launch_fwd_t<128, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                  : launch_fwd_t<128, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+  return causal ? launch_fwd_t<64, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                : launch_fwd_t<64, false>(tq, tk, tv, a, BH, grid_blocks, stream);
 }
 
 }  // namespace fa

@@ -44,7 +44,7 @@ struct BwdArgs {
 // Each returns the launch error (cudaSuccess on success).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                       bool causal, cudaStream_t stream);
+                       bool causal, int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
                            cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
