@@ -206,8 +206,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
   a.lse = lse;
   a.BH = BH;
   a.N = N;
-  // Re-read per head: its K and V.
-  a.group = heads_per_group(BH, (size_t)4 * N * d);
+  a.group = BH;  // the forward schedules over all heads at once
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = g_timeout_ns.load();

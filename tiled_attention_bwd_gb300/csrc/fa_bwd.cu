@@ -553,38 +553,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // D_i = dO_i . O_i and LSE2_i = LSE_i log2(e) for every padded row (one warp
-// per row); then the dQ accumulator is cleared.
+// per row, four rows in flight per warp); then the dQ accumulator is cleared.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  constexpr int kRows = 4;
+  constexpr int kPer = D / 32;  // 4 (d=128) or 2 (d=64) elements per lane
   const int lane = threadIdx.x & 31;
   const long long warps_total = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long gwarp = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long rows = (long long)a.BH * a.N_pad;
-  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       row < rows; row += warps_total) {
-    const int bh = (int)(row / a.N_pad);
-    const int q = (int)(row % a.N_pad);
-    float dsum = 0.f, l2 = INFINITY;
-    if (q < a.N) {
-      const size_t base = ((size_t)bh * a.N + q) * D;
-      constexpr int kPer = D / 32;  // 4 (d=128) or 2 (d=64) elements per lane
-      if constexpr (kPer == 4) {
-        const uint2 ov = *reinterpret_cast<const uint2*>(a.o + base + lane * 4);
-        const uint2 dv = *reinterpret_cast<const uint2*>(a.dout + base + lane * 4);
-        dsum = bf16_lo(ov.x) * bf16_lo(dv.x) + bf16_hi(ov.x) * bf16_hi(dv.x) +
-               bf16_lo(ov.y) * bf16_lo(dv.y) + bf16_hi(ov.y) * bf16_hi(dv.y);
-      } else {
-        const uint32_t ov = *reinterpret_cast<const uint32_t*>(a.o + base + lane * 2);
-        const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dout + base + lane * 2);
-        dsum = bf16_lo(ov) * bf16_lo(dv) + bf16_hi(ov) * bf16_hi(dv);
+  for (long long row0 = gwarp * kRows; row0 < rows; row0 += warps_total * kRows) {
+    uint32_t ov[kRows][kPer / 2], dv[kRows][kPer / 2];
+    bool valid[kRows];
+    long long lrow[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const long long row = row0 + k;
+      const int bh = (int)(row / a.N_pad);
+      const int q = (int)(row - (long long)bh * a.N_pad);
+      valid[k] = row < rows && q < a.N;
+      lrow[k] = (long long)bh * a.N + q;
+#pragma unroll
+      for (int e = 0; e < kPer / 2; ++e) ov[k][e] = dv[k][e] = 0u;
+      if (valid[k]) {
+        const size_t base = (size_t)lrow[k] * D + lane * kPer;
+        if constexpr (kPer == 4) {
+          const uint2 o2 = *reinterpret_cast<const uint2*>(a.o + base);
+          const uint2 d2 = *reinterpret_cast<const uint2*>(a.dout + base);
+          ov[k][0] = o2.x; ov[k][1] = o2.y;
+          dv[k][0] = d2.x; dv[k][1] = d2.y;
+        } else {
+          ov[k][0] = *reinterpret_cast<const uint32_t*>(a.o + base);
+          dv[k][0] = *reinterpret_cast<const uint32_t*>(a.dout + base);
+        }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      float dsum = 0.f;
+#pragma unroll
+      for (int e = 0; e < kPer / 2; ++e)
+        dsum += bf16_lo(ov[k][e]) * bf16_lo(dv[k][e]) + bf16_hi(ov[k][e]) * bf16_hi(dv[k][e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
         dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-      l2 = a.lse[(size_t)bh * a.N + q] * kLog2e;
-    }
-    if (lane == 0) {
-      a.ddot[row] = dsum;
-      a.lse2[row] = l2;
+      const long long row = row0 + k;
+      if (lane == 0 && row < rows) {
+        a.ddot[row] = valid[k] ? dsum : 0.f;
+        a.lse2[row] = valid[k] ? a.lse[lrow[k]] * kLog2e : INFINITY;
+      }
     }
   }
   const long long n4 = (long long)a.BH * a.N * D / 4;

@@ -112,8 +112,9 @@ struct FwdItem {
   int bh, qt0, qt1, nkv0, nkv1, nkv;
 };
 // Items are ordered heaviest first over the whole grid (pair index slow,
-// head fast; causal pairs from the last one down).  The forward re-reads
-// little, so global balance matters more here than L2 grouping by head.
+// head fast; causal pairs from the last one down).  Measured: grouping heads
+// so that their K/V stay in L2 cut DRAM reads but cost more in balance than
+// it saved, so the forward uses the global order.
 template <bool CAUSAL>
 __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
                                             int BH) {
