@@ -47,6 +47,25 @@ def load_peaks():
         return (FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback")
 
 
+def committed_traffic(kernel):
+    """DRAM bytes per launch of `kernel` at the headline workload, from the
+    committed ncu capture in profiles/traffic.json, if the kernel's sources
+    still hash to the fingerprint recorded with it; else None."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)["kernels"][kernel]
+        h = hashlib.sha256()
+        for path in rec["files"]:
+            with open(os.path.join(ROOT, path), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["fingerprint"]:
+            return None
+        return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"]), rec["workload"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -301,6 +320,8 @@ def run_ours(args, w, rank, world, local):
                "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    traffic = committed_traffic("bwd_main_kernel")
+    traffic_bytes = traffic[0] if traffic and traffic[1] == w.name else None
     step_flops = w.fwd_flops() + w.bwd_flops()
     value = world * step_flops / (step_ms * 1e-3) / 1e12
     fwd_tflops = world * w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
@@ -310,12 +331,12 @@ def run_ours(args, w, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         cores = oracle.num_threads()
-        rows = 512
-        f, s_ = oracle_sample(w, cores, rows)
+        heads = 2 * cores          # about 10 s of fp64 work at 4096x128
+        f, s_ = oracle_sample(w, heads, w.N)
         cpu = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores,
                "kind": "oracle",
-               "sample": "last %d query rows of %d heads of %s, fwd+bwd, "
-                         "%.1f s" % (rows, cores, w.name, s_)}
+               "sample": "all %d query rows of %d heads of %s, fwd+bwd, "
+                         "%.1f s" % (w.N, heads, w.name, s_)}
 
     if rank != 0:
         return
@@ -337,8 +358,11 @@ def run_ours(args, w, rank, world, local):
         "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor",
                      "achieved": main_tflops, "peak": peak_burst,
                      "unit": "TFLOP/s", "frac": main_tflops / peak_burst,
-                     "peak_source": "%s bf16 burst" % peak_src,
-                     "ms_per_launch": main_ms, "traffic": None},
+                     "peak_source": "%s bf16 burst (clocks stay at max: "
+                                    "not power-capped)" % peak_src,
+                     "ms_per_launch": main_ms, "traffic": traffic_bytes,
+                     "traffic_unit": "bytes per launch (ncu dram read+write)",
+                     "algorithmic_flop_per_launch": w.bwd_flops()},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * K,

@@ -1,0 +1,80 @@
+"""Host-side logic of bench.py (CPU only).
+
+* The timing reduction across ranks (max over ranks, as the benchmark takes
+  the slowest rank's time) is checked with two gloo processes on CPU.
+* The committed traffic record is only used while the kernel sources still
+  match the fingerprint stored with it.
+"""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        value = bench.max_over_ranks(1.5 + rank, world)
+        out[rank] = value
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_processes():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert out[0] == pytest.approx(2.5) and out[1] == pytest.approx(2.5)
+
+
+def test_single_process_timing_is_identity():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_committed_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    rec = bench.committed_traffic("bwd_main_kernel")
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        doc = json.load(f)
+    k = doc["kernels"]["bwd_main_kernel"]
+    if rec is not None:
+        assert rec[0] == k["dram_read_bytes"] + k["dram_write_bytes"]
+    # A copy of the repo whose source differs must not report traffic.
+    fake = tmp_path / "repo"
+    (fake / "profiles").mkdir(parents=True)
+    (fake / "profiles" / "traffic.json").write_text(json.dumps(doc))
+    for path in k["files"]:
+        dst = fake / path
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        dst.write_bytes(open(os.path.join(ROOT, path), "rb").read() + b"\n// edit")
+    monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.committed_traffic("bwd_main_kernel") is None
+
+
+def test_workload_flop_convention():
+    from tiled_attention_bwd_gb300.workloads import WORKLOADS
+    w = WORKLOADS["xl_4x64x4096x128_causal"]
+    assert w.fwd_flops() == pytest.approx(4 * 4 * 64 * 4096 ** 2 * 128 / 2)
+    assert w.bwd_flops() == pytest.approx(2.5 * w.fwd_flops())
