@@ -20,6 +20,12 @@ What each function follows:
   fwd_rows, bwd_rows -- the same computations restricted to a range of
                  query rows (rows are independent), so that long sequences can
                  be checked on rows the oracle finishes quickly.
+  fwd_ext, bwd_ext -- grouped / multi-query K/V heads (query head h reads
+                 K/V head h // (H // Hkv); dK, dV summed over each group) and
+                 a sliding window (key j visible to query i only if
+                 |i - j| <= window, and j <= i when causal).  The pages list
+                 both as future variants ("Advanced Features (Future)":
+                 multi-query / grouped query attention; sliding window).
   bwd         -- gradients dQ, dK, dV of L with dL/dO = dout, P recomputed
                  from the row's LSE ("GPU Performance Optimization Batch 1 --
                  Design Spec", Item 3, backward paragraph).  The formulas come
@@ -63,6 +69,15 @@ def _load():
                                         ctypes.c_int, ctypes.c_double, i64,
                                         i64, dp, dp, dp]
         lib.oracle_bwd_rows.restype = None
+        lib.oracle_fwd_ext_rows.argtypes = [dp, dp, dp, i64, i64, i64, i64,
+                                            i64, ctypes.c_int, i64,
+                                            ctypes.c_double, i64, i64, dp, dp]
+        lib.oracle_fwd_ext_rows.restype = None
+        lib.oracle_bwd_ext_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64,
+                                            i64, i64, ctypes.c_int, i64,
+                                            ctypes.c_double, i64, i64, dp, dp,
+                                            dp]
+        lib.oracle_bwd_ext_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -161,3 +176,46 @@ def bwd_rows(q, k, v, dout, causal: bool, scale: float, r0: int, r1: int):
                             int(bool(causal)), float(scale), int(r0), int(r1),
                             _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
+
+
+def _ext_shapes(q, k):
+    if q.ndim != 4 or k.ndim != 4:
+        raise ValueError("expected [B,H,N,d] q and [B,Hkv,N,d] k")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or Hkv < 1 or H % Hkv != 0:
+        raise ValueError("bad grouped shapes %s / %s" % (q.shape, k.shape))
+    return B, H, Hkv, N, d
+
+
+def fwd_ext(q, k, v, causal: bool, scale: float, window: int = -1,
+            r0: int = 0, r1: int = None):
+    """Forward with Hkv = k.shape[1] key/value heads and an optional window
+    (window < 0: none).  Rows outside [r0, r1) are NaN."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, Hkv, N, d = _ext_shapes(q, k)
+    r1 = N if r1 is None else r1
+    o = np.full_like(q, np.nan)
+    lse = np.full(q.shape[:-1], np.nan, dtype=np.float64)
+    _load().oracle_fwd_ext_rows(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, N, d,
+                                int(bool(causal)), int(window), float(scale),
+                                int(r0), int(r1), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def bwd_ext(q, k, v, dout, causal: bool, scale: float, window: int = -1,
+            r0: int = 0, r1: int = None):
+    """Backward of fwd_ext: dQ [B,H,N,d]; dK, dV [B,Hkv,N,d] summed over each
+    group of query heads.  Only query rows in [r0, r1) contribute."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, H, Hkv, N, d = _ext_shapes(q, k)
+    r1 = N if r1 is None else r1
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(k)
+    _load().oracle_bwd_ext_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H,
+                                Hkv, N, d, int(bool(causal)), int(window),
+                                float(scale), int(r0), int(r1), _ptr(dq),
+                                _ptr(dk), _ptr(dv))
+    return dq, dk, dv
+

@@ -56,26 +56,48 @@ static double dot(const double* a, const double* b, int64_t d) {
   return s;
 }
 
-/* Number of keys visible to query row i. */
+/* Number of keys visible to query row i (no window). */
 static int64_t visible_keys(int64_t i, int64_t n, int causal) {
   return causal ? (i + 1) : n;
 }
 
 /*
+ * Keys visible to query row i: lo <= j < hi.  Causal: j <= i.  A window
+ * w >= 0 (local attention) further keeps only |i - j| <= w; w < 0 means no
+ * window.
+ */
+static void visible_range(int64_t i, int64_t n, int causal, int64_t window,
+                          int64_t* lo, int64_t* hi) {
+  int64_t a = 0, b = causal ? i + 1 : n;
+  if (window >= 0) {
+    if (i - window > a) a = i - window;
+    if (!causal && i + window + 1 < b) b = i + window + 1;
+  }
+  *lo = a;
+  *hi = b;
+}
+
+/*
  * Scores s_j = scale * q_i . k_j for the visible keys, then the two-pass
  * log-sum-exp: m = max_j s_j, Z = sum_j exp(s_j - m), lse = m + ln Z.
- * Returns lse; s[] holds the scores.
+ * Returns lse; s[] holds the scores (s[0] is key `lo`).
  */
-static double row_scores_lse(const double* qi, const double* k, int64_t nvis,
-                             int64_t d, double scale, double* s) {
+static double row_scores_lse_range(const double* qi, const double* k,
+                                   int64_t lo, int64_t hi, int64_t d,
+                                   double scale, double* s) {
   double m = -INFINITY;
-  for (int64_t j = 0; j < nvis; ++j) {
-    s[j] = scale * dot(qi, k + j * d, d);
-    if (s[j] > m) m = s[j];
+  for (int64_t j = lo; j < hi; ++j) {
+    s[j - lo] = scale * dot(qi, k + j * d, d);
+    if (s[j - lo] > m) m = s[j - lo];
   }
   double z = 0.0;
-  for (int64_t j = 0; j < nvis; ++j) z += exp(s[j] - m);
+  for (int64_t j = lo; j < hi; ++j) z += exp(s[j - lo] - m);
   return m + log(z);
+}
+
+static double row_scores_lse(const double* qi, const double* k, int64_t nvis,
+                             int64_t d, double scale, double* s) {
+  return row_scores_lse_range(qi, k, 0, nvis, d, scale, s);
 }
 
 /*
@@ -251,3 +273,111 @@ void oracle_bwd(const double* q, const double* k, const double* v,
                 int causal, double scale, double* dq, double* dk, double* dv) {
   oracle_bwd_rows(q, k, v, dout, BH, N, d, causal, scale, 0, N, dq, dk, dv);
 }
+
+/*
+ * Grouped / multi-query attention with an optional sliding window.
+ * q, o: [B, H, N, d]; k, v: [B, Hkv, N, d] with H % Hkv == 0; query head h
+ * reads key/value head h / (H / Hkv).  Visible keys as in visible_range.
+ * Rows r0 <= i < r1 only (the other rows of o and lse are untouched).
+ */
+void oracle_fwd_ext_rows(const double* q, const double* k, const double* v,
+                         int64_t B, int64_t H, int64_t Hkv, int64_t N,
+                         int64_t d, int causal, int64_t window, double scale,
+                         int64_t r0, int64_t r1, double* o, double* lse) {
+  const int64_t group = H / Hkv;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+      const int64_t b = bh / H, h = bh % H;
+      const int64_t bkv = b * Hkv + h / group;
+      const double* qh = q + bh * N * d;
+      const double* kh = k + bkv * N * d;
+      const double* vh = v + bkv * N * d;
+      double* oh = o + bh * N * d;
+      for (int64_t i = r0; i < r1; ++i) {
+        int64_t lo, hi;
+        visible_range(i, N, causal, window, &lo, &hi);
+        const double l = row_scores_lse_range(qh + i * d, kh, lo, hi, d, scale, s);
+        lse[bh * N + i] = l;
+        double* oi = oh + i * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        for (int64_t j = lo; j < hi; ++j) {
+          const double p = exp(s[j - lo] - l);
+          const double* vj = vh + j * d;
+          for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
+        }
+      }
+    }
+    free(s);
+  }
+}
+
+/*
+ * Backward of the grouped / windowed forward: dq [B, H, N, d] per query
+ * head; dk, dv [B, Hkv, N, d] summed over the query heads of each group
+ * (each head's contribution is the chain rule of its own softmax, as in
+ * oracle_bwd).  Query rows r0 <= i < r1 only contribute.  Work is split by
+ * key/value head so that no two threads add into the same dk/dv rows.
+ */
+void oracle_bwd_ext_rows(const double* q, const double* k, const double* v,
+                         const double* dout, int64_t B, int64_t H, int64_t Hkv,
+                         int64_t N, int64_t d, int causal, int64_t window,
+                         double scale, int64_t r0, int64_t r1, double* dq,
+                         double* dk, double* dv) {
+  const int64_t group = H / Hkv;
+  memset(dq, 0, sizeof(double) * (size_t)(B * H * N * d));
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double* oi = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bkv = 0; bkv < B * Hkv; ++bkv) {
+      const int64_t b = bkv / Hkv, g = bkv % Hkv;
+      const double* kh = k + bkv * N * d;
+      const double* vh = v + bkv * N * d;
+      double* dkh = dk + bkv * N * d;
+      double* dvh = dv + bkv * N * d;
+      memset(dkh, 0, sizeof(double) * (size_t)(N * d));
+      memset(dvh, 0, sizeof(double) * (size_t)(N * d));
+      for (int64_t h = g * group; h < (g + 1) * group; ++h) {
+        const int64_t bh = b * H + h;
+        const double* qh = q + bh * N * d;
+        const double* doh = dout + bh * N * d;
+        double* dqh = dq + bh * N * d;
+        for (int64_t i = r0; i < r1; ++i) {
+          int64_t lo, hi;
+          visible_range(i, N, causal, window, &lo, &hi);
+          const double* qi = qh + i * d;
+          const double* doi = doh + i * d;
+          const double l = row_scores_lse_range(qi, kh, lo, hi, d, scale, s);
+          for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+          for (int64_t j = lo; j < hi; ++j) {
+            s[j - lo] = exp(s[j - lo] - l); /* now P_ij */
+            const double* vj = vh + j * d;
+            for (int64_t t = 0; t < d; ++t) oi[t] += s[j - lo] * vj[t];
+          }
+          const double D = dot(doi, oi, d);
+          double* dqi = dqh + i * d;
+          for (int64_t j = lo; j < hi; ++j) {
+            const double p = s[j - lo];
+            const double* kj = kh + j * d;
+            const double* vj = vh + j * d;
+            const double ds = p * (dot(doi, vj, d) - D);
+            double* dkj = dkh + j * d;
+            double* dvj = dvh + j * d;
+            for (int64_t t = 0; t < d; ++t) {
+              dqi[t] += scale * ds * kj[t];
+              dkj[t] += scale * ds * qi[t];
+              dvj[t] += p * doi[t];
+            }
+          }
+        }
+      }
+    }
+    free(oi);
+    free(s);
+  }
+}
+

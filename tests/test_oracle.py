@@ -254,3 +254,149 @@ def test_row_ranges_agree_with_full_computation(causal):
         _, dk_t, dv_t = oracle.bwd_rows(q, k, v, do, True, 0.3, 60, 90)
         np.testing.assert_allclose(dk_t[:, :, 60:], dk[:, :, 60:], atol=1e-14)
         np.testing.assert_allclose(dv_t[:, :, 60:], dv[:, :, 60:], atol=1e-14)
+
+
+# ---------------------------------------------- grouped heads, sliding window
+def _torch_reference_ext(q, k, v, do, causal, scale, window):
+    """Grouped / windowed attention with torch fp64 autograd: K/V heads are
+    repeated to the query heads (so autograd sums dK/dV over each group) and
+    the band is an explicit mask."""
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
+                  for x in (q, k, v))
+    group = q.shape[1] // k.shape[1]
+    kk = tk.repeat_interleave(group, dim=1)
+    vv = tv.repeat_interleave(group, dim=1)
+    s = scale * tq @ kk.transpose(-1, -2)
+    n = s.shape[-1]
+    i = torch.arange(n)[:, None]
+    j = torch.arange(n)[None, :]
+    hidden = torch.zeros(n, n, dtype=torch.bool)
+    if causal:
+        hidden |= j > i
+    if window >= 0:
+        hidden |= (i - j) > window
+        if not causal:
+            hidden |= (j - i) > window
+    s = s.masked_fill(hidden, float("-inf"))
+    p = torch.softmax(s, dim=-1)
+    o = p @ vv
+    lse = torch.logsumexp(s, dim=-1)
+    o.backward(torch.tensor(do, dtype=torch.float64))
+    return (o.detach().numpy(), lse.detach().numpy(), tq.grad.numpy(),
+            tk.grad.numpy(), tv.grad.numpy())
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (6, 1)])
+@pytest.mark.parametrize("window", [-1, 0, 3, 40])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ext_matches_torch_autograd(H, Hkv, window, causal):
+    B, N, d = 2, 37, 8
+    q, do = _rand((B, H, N, d), 201), _rand((B, H, N, d), 202)
+    k, v = _rand((B, Hkv, N, d), 203), _rand((B, Hkv, N, d), 204)
+    ref = _torch_reference_ext(q, k, v, do, causal, 0.4, window)
+    o, lse = oracle.fwd_ext(q, k, v, causal, 0.4, window=window)
+    grads = oracle.bwd_ext(q, k, v, do, causal, 0.4, window=window)
+    for got, want in zip((o, lse) + grads, ref):
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("window", [0, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ext_gradients_match_finite_differences(window, causal):
+    B, H, Hkv, N, d = 1, 2, 1, 6, 3
+    q, do = _rand((B, H, N, d), 211), _rand((B, H, N, d), 212)
+    k, v = _rand((B, Hkv, N, d), 213), _rand((B, Hkv, N, d), 214)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.fwd_ext(qq, kk, vv, causal, 0.6, window=window)
+        return float(np.sum(o * do))
+
+    grads = oracle.bwd_ext(q, k, v, do, causal, 0.6, window=window)
+    h = 1e-6
+    for which, g in zip(range(3), grads):
+        args = [q, k, v]
+        fd = np.zeros(args[which].shape)
+        for idx in np.ndindex(*fd.shape):
+            ap = [a.copy() for a in args]
+            am = [a.copy() for a in args]
+            ap[which][idx] += h
+            am[which][idx] -= h
+            fd[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+        err = np.linalg.norm(g - fd) / max(np.linalg.norm(fd), 1e-12)
+        assert err < 1e-6 or np.max(np.abs(g - fd)) < 1e-8, (which, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ext_without_groups_or_window_is_the_base_operation(causal):
+    shape = (2, 3, 50, 8)
+    q, k, v, do = (_rand(shape, 220 + s) for s in range(4))
+    o1, l1 = oracle.fwd(q, k, v, causal, 0.3)
+    o2, l2 = oracle.fwd_ext(q, k, v, causal, 0.3, window=-1)
+    o3, l3 = oracle.fwd_ext(q, k, v, causal, 0.3, window=50)  # window >= N
+    np.testing.assert_allclose(o2, o1, atol=1e-15)
+    np.testing.assert_allclose(l2, l1, atol=1e-15)
+    np.testing.assert_allclose(o3, o1, atol=1e-15)
+    g1 = oracle.bwd(q, k, v, do, causal, 0.3)
+    g2 = oracle.bwd_ext(q, k, v, do, causal, 0.3, window=-1)
+    for a, b in zip(g2, g1):
+        np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+def test_causal_window_zero_sees_only_the_diagonal():
+    shape = (1, 2, 20, 8)
+    q, k, v = _rand(shape, 231), _rand(shape, 232), _rand(shape, 233)
+    o, lse = oracle.fwd_ext(q, k, v, True, 0.5, window=0)
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.5 * np.sum(q * k, -1), atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_band_of_the_probability_matrix(causal):
+    # V = identity makes O the probability matrix: zero outside the band,
+    # rows summing to one.
+    N, w = 24, 5
+    q, k = _rand((1, 1, N, N), 241), _rand((1, 1, N, N), 242)
+    v = np.eye(N).reshape(1, 1, N, N)
+    p, _ = oracle.fwd_ext(q, k, v, causal, 0.3, window=w)
+    p = p[0, 0]
+    i, j = np.indices((N, N))
+    outside = (i - j > w) | ((j - i > w) if not causal else (j > i))
+    assert np.all(p[outside] == 0.0)
+    assert np.all(p[~outside] > 0.0)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_equal_repeated_heads(causal):
+    # Hkv < H equals the plain operation on K/V repeated per query head,
+    # with dK/dV summed over each group (no torch involved).
+    B, H, Hkv, N, d = 2, 6, 2, 30, 8
+    q, do = _rand((B, H, N, d), 251), _rand((B, H, N, d), 252)
+    k, v = _rand((B, Hkv, N, d), 253), _rand((B, Hkv, N, d), 254)
+    kr, vr = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
+    o1, l1 = oracle.fwd_ext(q, k, v, causal, 0.3, window=7)
+    o2, l2 = oracle.fwd_ext(q, kr, vr, causal, 0.3, window=7)
+    np.testing.assert_allclose(o1, o2, atol=1e-15)
+    np.testing.assert_allclose(l1, l2, atol=1e-15)
+    dq1, dk1, dv1 = oracle.bwd_ext(q, k, v, do, causal, 0.3, window=7)
+    dq2, dk2, dv2 = oracle.bwd_ext(q, kr, vr, do, causal, 0.3, window=7)
+    np.testing.assert_allclose(dq1, dq2, atol=1e-14)
+    g = H // Hkv
+    np.testing.assert_allclose(dk1, dk2.reshape(B, Hkv, g, N, d).sum(2), atol=1e-13)
+    np.testing.assert_allclose(dv1, dv2.reshape(B, Hkv, g, N, d).sum(2), atol=1e-13)
+
+
+def test_ext_row_ranges():
+    B, H, Hkv, N, d = 1, 4, 2, 40, 8
+    q, do = _rand((B, H, N, d), 261), _rand((B, H, N, d), 262)
+    k, v = _rand((B, Hkv, N, d), 263), _rand((B, Hkv, N, d), 264)
+    o, lse = oracle.fwd_ext(q, k, v, True, 0.3, window=9)
+    o_r, lse_r = oracle.fwd_ext(q, k, v, True, 0.3, window=9, r0=10, r1=25)
+    np.testing.assert_allclose(o_r[:, :, 10:25], o[:, :, 10:25], atol=1e-15)
+    assert np.isnan(o_r[:, :, :10]).all() and np.isnan(lse_r[:, :, 25:]).all()
+    dq, dk, dv = oracle.bwd_ext(q, k, v, do, True, 0.3, window=9)
+    a = oracle.bwd_ext(q, k, v, do, True, 0.3, window=9, r0=0, r1=20)
+    b = oracle.bwd_ext(q, k, v, do, True, 0.3, window=9, r0=20, r1=40)
+    np.testing.assert_allclose(a[0] + b[0], dq, atol=1e-14)
+    np.testing.assert_allclose(a[1] + b[1], dk, atol=1e-13)
+    np.testing.assert_allclose(a[2] + b[2], dv, atol=1e-13)
