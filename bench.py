@@ -1,6 +1,7 @@
 """Benchmark: attention forward + backward TFLOP/s on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--hkv HKV] [--window W]
                     [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
 
 One step = fa_fwd + fa_bwd over the whole workload (default: 4x64x4096x128
@@ -10,7 +11,10 @@ reported value is the total algorithmic FLOPs of all ranks divided by the
 slowest rank's time.  Rank 0 prints one JSON line.
 
 FLOP convention: forward = 4 B H N^2 d (halved when causal), backward = 2.5 x
-forward, step = 3.5 x forward.
+forward, step = 3.5 x forward.  With --window the N^2 (or N^2 / 2) becomes
+the number of visible (query, key) pairs of the band.  --hkv runs the
+grouped-query variant (K/V heads shared by H / HKV query heads); it does not
+change the FLOPs.
 
 --impl reference times the CPU fp64 oracle (the plain definition, no tuning)
 on the host cores, each step a bounded sample of the same workload (the last
@@ -154,25 +158,49 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def oracle_sample(w, heads, rows):
+def oracle_sample(w, heads, rows, window=-1):
     """Run the CPU oracle (forward + backward) on the last `rows` query rows
-    of `heads` heads of workload `w`.  Returns (algorithmic FLOPs, seconds)."""
-    import numpy as np
+    of `heads` heads of workload `w` (with a window: each head as a batch
+    entry of its own, which is the per-head arithmetic of the grouped
+    operation too).  Returns (algorithmic FLOPs, seconds)."""
     import oracle
-    from tiled_attention_bwd_gb300.workloads import make_inputs
+    from tiled_attention_bwd_gb300.workloads import make_inputs, visible_pairs
     inp = make_inputs(1, heads, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
-    q, k, v, do = (inp[n].double().numpy()[0] for n in ("q", "k", "v", "do"))
     r0 = w.N - rows
-    t0 = time.perf_counter()
-    oracle.fwd_rows(q, k, v, w.causal, w.scale, r0, w.N)
-    oracle.bwd_rows(q, k, v, do, w.causal, w.scale, r0, w.N)
-    dt = time.perf_counter() - t0
-    if w.causal:
-        pairs = float(np.sum(np.arange(r0, w.N) + 1))
+    if window < 0:
+        q, k, v, do = (inp[n].double().numpy()[0] for n in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        oracle.fwd_rows(q, k, v, w.causal, w.scale, r0, w.N)
+        oracle.bwd_rows(q, k, v, do, w.causal, w.scale, r0, w.N)
     else:
-        pairs = float(rows) * w.N
+        q, k, v, do = (inp[n].double().numpy().transpose(1, 0, 2, 3)
+                       for n in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        oracle.fwd_ext(q, k, v, w.causal, w.scale, window, r0, w.N)
+        oracle.bwd_ext(q, k, v, do, w.causal, w.scale, window, r0, w.N)
+    dt = time.perf_counter() - t0
+    pairs = float(visible_pairs(w.N, w.causal, window, r0, w.N))
     flops = heads * pairs * 4.0 * w.d * 3.5
     return flops, dt
+
+
+def step_flops(w, window):
+    """Algorithmic FLOPs of one forward (and of one backward = 2.5 x)."""
+    from tiled_attention_bwd_gb300.workloads import visible_pairs
+    if window < 0:
+        return w.fwd_flops(), w.bwd_flops()
+    f = 4.0 * w.B * w.H * w.d * visible_pairs(w.N, w.causal, window)
+    return f, 2.5 * f
+
+
+def variant_config(w, args):
+    """config keys of the grouped-head / window variant (empty if none)."""
+    c = {}
+    if args.hkv is not None:
+        c["Hkv"] = args.hkv
+    if args.window >= 0:
+        c["window"] = args.window
+    return c
 
 
 def run_reference(args, w, rank, world):
@@ -183,10 +211,10 @@ def run_reference(args, w, rank, world):
     cores = oracle.num_threads()
     rows = 128
     for _ in range(args.warmup):
-        oracle_sample(w, cores, rows)
+        oracle_sample(w, cores, rows, args.window)
     total_flops, total_s = 0.0, 0.0
     for _ in range(args.steps):
-        f, s = oracle_sample(w, cores, rows)
+        f, s = oracle_sample(w, cores, rows, args.window)
         total_flops += f
         total_s += s
     value = total_flops / total_s / 1e12
@@ -198,8 +226,9 @@ def run_reference(args, w, rank, world):
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                   "d": w.d, "causal": w.causal},
+        "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                        "d": w.d, "causal": w.causal},
+                       **variant_config(w, args)),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -210,30 +239,39 @@ def run_reference(args, w, rank, world):
 
 def run_ours(args, w, rank, world, local):
     import torch
-    from tiled_attention_bwd_gb300 import (fa_bwd, fa_bwd_set_phase_events,
-                                           fa_bwd_workspace_size,
-                                           fa_check_device_status, fa_fwd,
+    from tiled_attention_bwd_gb300 import (fa_bwd_ext, fa_bwd_set_phase_events,
+                                           fa_bwd_ext_workspace_size,
+                                           fa_check_device_status, fa_fwd_ext,
                                            load_library)
-    from tiled_attention_bwd_gb300.workloads import workload_inputs
+    from tiled_attention_bwd_gb300.workloads import make_grouped_inputs
 
     load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peak_burst, peak_sust, hbm_peak, peak_src = load_peaks()
 
-    inp_cpu = workload_inputs(w)
+    # fa_fwd / fa_bwd are fa_fwd_ext / fa_bwd_ext with Hkv = H and no
+    # window; the same draw order makes Hkv = H identical to the base inputs.
+    hkv = w.H if args.hkv is None else args.hkv
+    window = args.window
+    inp_cpu = make_grouped_inputs(w.B, w.H, hkv, w.N, w.d, w.seed, w.qk_mult)
     q, k, v, do = (inp_cpu[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    ws = torch.empty(fa_bwd_workspace_size(w.B, w.H, w.N, w.d),
+    dq = torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa_bwd_ext_workspace_size(w.B, w.H, hkv, w.N, w.d),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    fwd_flops, bwd_flops = step_flops(w, window)
+
+    def fwd():
+        fa_fwd_ext(q, k, v, w.causal, w.scale, window, out=o, lse=lse)
 
     def step():
-        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
-        fa_bwd(q, k, v, o, lse, do, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
-               workspace=ws)
+        fwd()
+        fa_bwd_ext(q, k, v, o, lse, do, w.causal, w.scale, window, dq=dq,
+                   dk=dk, dv=dv, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -275,11 +313,11 @@ def run_ours(args, w, rank, world, local):
     fw_s = torch.cuda.Event(enable_timing=True)
     fw_e = torch.cuda.Event(enable_timing=True)
     for _ in range(max(1, args.warmup)):
-        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+        fwd()
     torch.cuda.synchronize(dev)
     fw_s.record(stream)
     for _ in range(K):
-        fa_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+        fwd()
     fw_e.record(stream)
     torch.cuda.synchronize(dev)
     fwd_ms = max_over_ranks(fw_s.elapsed_time(fw_e) / K, world, dev)
@@ -316,23 +354,23 @@ def run_ours(args, w, rank, world, local):
         h2d = sum(host[n].numel() * host[n].element_size() for n in host)
         d2h = (sum(outs[n].numel() * outs[n].element_size() for n in outs)
                + lse_h.numel() * 4)
-        e2e = {"value": world * (w.fwd_flops() + w.bwd_flops()) / (e2e_ms * 1e-3) / 1e12,
+        e2e = {"value": world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     traffic = committed_traffic("bwd_main_kernel")
-    traffic_bytes = traffic[0] if traffic and traffic[1] == w.name else None
-    step_flops = w.fwd_flops() + w.bwd_flops()
-    value = world * step_flops / (step_ms * 1e-3) / 1e12
-    fwd_tflops = world * w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
-    main_tflops = w.bwd_flops() / (main_ms * 1e-3) / 1e12
+    traffic_bytes = (traffic[0] if traffic and traffic[1] == w.name
+                     and not variant_config(w, args) else None)
+    value = world * (fwd_flops + bwd_flops) / (step_ms * 1e-3) / 1e12
+    fwd_tflops = world * fwd_flops / (fwd_ms * 1e-3) / 1e12
+    main_tflops = bwd_flops / (main_ms * 1e-3) / 1e12
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         cores = oracle.num_threads()
         heads = 2 * cores          # about 10 s of fp64 work at 4096x128
-        f, s_ = oracle_sample(w, heads, w.N)
+        f, s_ = oracle_sample(w, heads, w.N, window)
         cpu = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores,
                "kind": "oracle",
                "sample": "all %d query rows of %d heads of %s, fwd+bwd, "
@@ -345,11 +383,13 @@ def run_ours(args, w, rank, world, local):
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                   "d": w.d, "causal": w.causal, "scale": w.scale,
-                   "qk_mult": w.qk_mult, "per_gpu": "full workload per rank",
-                   "l2": "inputs larger than L2 (%d MB per tensor)" % (
-                       q.numel() * 2 // 2**20)},
+        "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                        "d": w.d, "causal": w.causal, "scale": w.scale,
+                        "qk_mult": w.qk_mult,
+                        "per_gpu": "full workload per rank",
+                        "l2": "inputs larger than L2 (%d MB per Q tensor)" % (
+                            q.numel() * 2 // 2**20)},
+                       **variant_config(w, args)),
         "fwd": {"value": fwd_tflops, "unit": "TFLOP/s", "ms": fwd_ms,
                 "frac_of_peak": fwd_tflops / world / peak_burst},
         "fwd_bwd_frac_of_peak": value / world / peak_burst,
@@ -362,7 +402,7 @@ def run_ours(args, w, rank, world, local):
                                     "not power-capped)" % peak_src,
                      "ms_per_launch": main_ms, "traffic": traffic_bytes,
                      "traffic_unit": "bytes per launch (ncu dram read+write)",
-                     "algorithmic_flop_per_launch": w.bwd_flops()},
+                     "algorithmic_flop_per_launch": bwd_flops},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * K,
@@ -378,6 +418,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--hkv", type=int, default=None,
+                    help="key/value heads (divides H; default H)")
+    ap.add_argument("--window", type=int, default=-1,
+                    help="sliding window |i - j| <= W (default: none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -385,6 +429,8 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.hkv is not None and (args.hkv < 1 or w.H % args.hkv != 0):
+        raise SystemExit("--hkv must divide H = %d" % w.H)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, w, rank, world)

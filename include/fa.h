@@ -103,6 +103,46 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  int H, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * Grouped-query / multi-query attention and sliding-window attention, the
+ * variants listed under "Advanced Features (Future)" of "RTX Flash Attention
+ * Implementation COMPLETE" ("Multi-Query Attention: grouped query attention
+ * variants"; "Sliding Window: local attention").  Same operation and
+ * conventions as fa_fwd / fa_bwd, except:
+ *   - k, v (and dk, dv) have Hkv heads: bf16 [B,Hkv,N,d].  Query head h of a
+ *     batch entry reads key/value head h / (H / Hkv).  Hkv must divide H
+ *     (1 <= Hkv <= H); Hkv = 1 is multi-query attention, Hkv = H the plain
+ *     operation.  dk and dv are summed over the H / Hkv query heads that
+ *     share each key/value head.
+ *   - window >= 0 limits query i to keys j with |i - j| <= window (and
+ *     j <= i when causal = 1); window < 0 means no limit.  A window of N - 1
+ *     or more hides nothing.  The pages' "global tokens" are not defined
+ *     there and are not part of this operation.
+ *   - lse, o, dout, dq keep the query heads: [B,H,N] / [B,H,N,d].
+ * fa_bwd_ext needs fa_bwd_ext_workspace_size(B, H, Hkv, N, d) bytes of
+ * workspace (equal to fa_bwd_workspace_size(B, H, N, d) for Hkv = H).
+ * H % Hkv != 0, Hkv < 1 or Hkv > H (for H >= 1) is FA_ERR_INVALID_ARG.
+ * fa_fwd and fa_bwd are these calls with Hkv = H and window = -1.
+ */
+fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
+                     float* lse, int B, int H, int Hkv, int N, int d,
+                     int causal, int window, float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd_ext needs: the fa_bwd workspace plus,
+ * when more than 8 query heads share a key/value head (their backward is
+ * then split over several blocks), two fp32 [B,Hkv,N,d] accumulators for dK
+ * and dV.  Returns 0 for an empty problem, unsupported d or invalid Hkv.
+ */
+size_t fa_bwd_ext_workspace_size(int B, int H, int Hkv, int N, int d);
+
+fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N,
+                     int d, int causal, int window, float scale,
+                     void* stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device status record
  * of the current GPU: FA_ERR_DEVICE_TIMEOUT if any kernel of this library
  * gave up on a pipeline wait since the last check, FA_ERR_CUDA if the stream

@@ -78,3 +78,29 @@ def test_workload_flop_convention():
     w = WORKLOADS["xl_4x64x4096x128_causal"]
     assert w.fwd_flops() == pytest.approx(4 * 4 * 64 * 4096 ** 2 * 128 / 2)
     assert w.bwd_flops() == pytest.approx(2.5 * w.fwd_flops())
+
+
+def test_step_flops_of_the_band():
+    from tiled_attention_bwd_gb300.workloads import WORKLOADS, visible_pairs
+    w = WORKLOADS["xl_4x64x4096x128_causal"]
+    # No window: the N^2 / 2 convention of the base workload.
+    assert bench.step_flops(w, -1) == (w.fwd_flops(), w.bwd_flops())
+    f, b = bench.step_flops(w, 1024)
+    pairs = visible_pairs(w.N, True, 1024)
+    # causal band of half-width W: row i sees min(i, W) + 1 keys
+    assert pairs == sum(min(i, 1024) + 1 for i in range(w.N))
+    assert f == 4.0 * w.B * w.H * w.d * pairs and b == 2.5 * f
+    assert visible_pairs(10, False, 2, 3, 7) == 4 * 5
+
+
+def test_reference_arm_runs_with_a_window():
+    import subprocess
+    import sys
+    out = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+         "reference", "--steps", "1", "--warmup", "0", "--workload",
+         "small_2x8x512x64", "--window", "100", "--hkv", "2"],
+        capture_output=True, text=True, timeout=300, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["window"] == 100 and line["config"]["Hkv"] == 2

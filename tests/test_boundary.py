@@ -25,6 +25,7 @@ def lib():
 def test_header_declares_the_expected_entry_points():
     names = fa.header_functions()
     for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
+              "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_ext_workspace_size",
               "fa_check_device_status", "fa_status_string",
               "fa_set_wait_timeout_ns", "fa_debug_expire_wait"):
         assert n in names
@@ -121,3 +122,68 @@ def test_workspace_size(lib, B, H, N, d):
     expect = (_align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4))
     assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
     assert fa.fa_bwd_workspace_size(B, H, N, d) == expect
+
+
+def _fwd_ext(lib, ptr=16, lse=16, B=1, H=4, Hkv=2, N=128, d=128, causal=0,
+             window=-1, scale=0.125):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_fwd_ext(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), B, H, Hkv,
+                          N, d, causal, window, scale, None)
+
+
+def _bwd_ext(lib, ptr=16, ws=16, ws_bytes=1 << 40, B=1, H=4, Hkv=2, N=128,
+             d=128, causal=0, window=-1, scale=0.125, lse=16):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_bwd_ext(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), p(ptr),
+                          p(ptr), p(ptr), p(ptr), p(ws), ws_bytes, B, H, Hkv,
+                          N, d, causal, window, scale, None)
+
+
+def test_grouped_head_argument_checks(lib):
+    for call in (_fwd_ext, _bwd_ext):
+        assert call(lib, Hkv=0) == INVALID        # no key/value head
+        assert call(lib, Hkv=-1) == INVALID
+        assert call(lib, H=4, Hkv=3) == INVALID   # does not divide H
+        assert call(lib, H=4, Hkv=8) == INVALID   # more K/V than query heads
+        assert call(lib, d=96) == UNSUPPORTED
+        assert call(lib, scale=0.0) == INVALID
+        assert call(lib, causal=2) == INVALID
+        assert call(lib, ptr=0) == INVALID
+        assert call(lib, ptr=24) == INVALID
+        # Empty problems are no-ops whatever the window.
+        assert call(lib, ptr=0, lse=0, N=0, window=5) == OK
+        assert call(lib, ptr=0, lse=0, H=0, Hkv=0) == OK
+    assert _bwd_ext(lib, ws=0) == WORKSPACE
+    need = lib.fa_bwd_ext_workspace_size(1, 4, 2, 128, 128)
+    assert _bwd_ext(lib, ws_bytes=need - 1) == WORKSPACE
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d", [(4, 64, 64, 4096, 128),
+                                         (4, 64, 8, 4096, 128),
+                                         (4, 64, 1, 4096, 128),
+                                         (2, 12, 1, 333, 64),
+                                         (1, 16, 2, 1000, 128)])
+def test_grouped_workspace_size(lib, B, H, Hkv, N, d):
+    n_pad = _align(N, 128)
+    base = _align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4)
+    g = H // Hkv
+    hpb = max(h for h in range(1, min(g, 8) + 1) if g % h == 0)
+    extra = 2 * _align(B * Hkv * N * d * 4) if g // hpb > 1 else 0
+    assert lib.fa_bwd_ext_workspace_size(B, H, Hkv, N, d) == base + extra
+    if Hkv == H:
+        assert lib.fa_bwd_workspace_size(B, H, N, d) == base
+    assert lib.fa_bwd_ext_workspace_size(B, H, 3, N, d) == 0 or H % 3 == 0
+    assert lib.fa_bwd_ext_workspace_size(0, H, Hkv, N, d) == 0
+
+
+def test_python_binding_checks_grouped_shapes():
+    import torch
+    q = torch.zeros((1, 4, 8, 64), dtype=torch.bfloat16)
+    k = torch.zeros((1, 3, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa._check_ext_shapes(q, k)     # 3 does not divide 4
+    k = torch.zeros((1, 2, 9, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa._check_ext_shapes(q, k)     # sequence lengths differ
+    k = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16)
+    assert fa._check_ext_shapes(q, k) == (1, 4, 2, 8, 64)

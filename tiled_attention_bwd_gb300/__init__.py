@@ -4,12 +4,16 @@ The compute path is libfa.so (hand-written tcgen05/TMA kernels behind the C
 ABI of include/fa.h); this package only builds it, marshals arguments to it,
 and describes the synthetic workloads.
 """
-from .fa import (FAError, fa_bwd, fa_bwd_set_phase_events,
+from .fa import (FAError, fa_bwd, fa_bwd_ext, fa_bwd_ext_workspace_size,
+                 fa_bwd_noalloc,
+                 fa_bwd_noalloc_max_workspace, fa_bwd_set_phase_events,
                  fa_bwd_workspace_size, fa_check_device_status,
-                 fa_debug_expire_wait, fa_fwd, fa_set_wait_timeout_ns,
-                 fa_status_string, load_library)
+                 fa_debug_expire_wait, fa_fwd, fa_fwd_ext,
+                 fa_set_wait_timeout_ns, fa_status_string, load_library)
 
-__all__ = ["FAError", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
-           "fa_check_device_status", "fa_set_wait_timeout_ns",
-           "fa_debug_expire_wait", "fa_bwd_set_phase_events",
-           "fa_status_string", "load_library"]
+__all__ = ["FAError", "fa_fwd", "fa_bwd", "fa_fwd_ext", "fa_bwd_ext",
+           "fa_bwd_ext_workspace_size",
+           "fa_bwd_workspace_size", "fa_bwd_noalloc",
+           "fa_bwd_noalloc_max_workspace", "fa_check_device_status",
+           "fa_set_wait_timeout_ns", "fa_debug_expire_wait",
+           "fa_bwd_set_phase_events", "fa_status_string", "load_library"]

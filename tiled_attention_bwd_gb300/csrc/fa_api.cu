@@ -139,6 +139,16 @@ fa_status check_shape(int B, int H, int N, int d, int causal, float scale,
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Checks of the grouped-head / window arguments on top of check_shape.
+// H query heads share Hkv key/value heads (Hkv divides H); window < 0 means
+// no band.  A window of N - 1 or more hides nothing and is returned as -1.
+fa_status check_ext(int H, int Hkv, int N, int window, int* window_out) {
+  if (Hkv < 0) return FA_ERR_INVALID_ARG;
+  if (H > 0 && (Hkv == 0 || Hkv > H || H % Hkv != 0)) return FA_ERR_INVALID_ARG;
+  *window_out = (window < 0 || (long long)window >= (long long)N - 1) ? -1 : window;
+  return FA_OK;
+}
+
 // Heads per scheduling group: as many heads as keep `bytes_per_head` of
 // re-read data within an L2 budget, at least one.
 int heads_per_group(int BH, size_t bytes_per_head) {
@@ -149,18 +159,38 @@ int heads_per_group(int BH, size_t bytes_per_head) {
   return (int)g;
 }
 
+// Query heads per backward block: the largest divisor of the group size
+// H / Hkv not above kMaxHeadsPerBlock.  A larger group is split over
+// several blocks per (key/value head, key tile), which then sum dK, dV in
+// fp32 workspace.
+constexpr int kMaxHeadsPerBlock = 8;
+int heads_per_block(int qgroup) {
+  for (int h = qgroup < kMaxHeadsPerBlock ? qgroup : kMaxHeadsPerBlock; h > 1; --h)
+    if (qgroup % h == 0) return h;
+  return 1;
+}
+
 struct WsLayout {
-  size_t dq_acc_off, ddot_off, lse2_off, total;
+  size_t dq_acc_off, ddot_off, lse2_off, dk_acc_off, dv_acc_off, total;
+  int hpb, nsplit;
 };
 
-WsLayout ws_layout(int B, int H, int N, int d) {
-  const size_t BH = (size_t)B * H;
+// dQacc [B,H,N,d] | D [B*H, N_pad] | LSE2 [B*H, N_pad] (| dKacc, dVacc
+// [B,Hkv,N,d] when the group is split), each 256-byte aligned.
+WsLayout ws_layout(int B, int H, int Hkv, int N, int d) {
+  const size_t BH = (size_t)B * H, BHkv = (size_t)B * Hkv;
   const size_t n_pad = align_up((size_t)N, fa::kTile);
   WsLayout w;
+  const int qgroup = Hkv > 0 ? H / Hkv : 1;
+  w.hpb = heads_per_block(qgroup);
+  w.nsplit = qgroup / w.hpb;
   w.dq_acc_off = 0;
   w.ddot_off = align_up(BH * N * d * sizeof(float), 256);
   w.lse2_off = w.ddot_off + align_up(BH * n_pad * sizeof(float), 256);
-  w.total = w.lse2_off + align_up(BH * n_pad * sizeof(float), 256);
+  w.dk_acc_off = w.lse2_off + align_up(BH * n_pad * sizeof(float), 256);
+  const size_t kv_acc = w.nsplit > 1 ? align_up(BHkv * N * d * sizeof(float), 256) : 0;
+  w.dv_acc_off = w.dk_acc_off + kv_acc;
+  w.total = w.dv_acc_off + kv_acc;
   return w;
 }
 
@@ -184,28 +214,33 @@ void fa_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
 }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
-                 float* lse, int B, int H, int N, int d, int causal,
-                 float scale, void* stream) {
+fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
+                     float* lse, int B, int H, int Hkv, int N, int d,
+                     int causal, int window, float scale, void* stream) {
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
-  if (s != FA_OK || empty) return s;
+  if (s != FA_OK) return s;
+  int win = -1;
+  if ((s = check_ext(H, Hkv, N, window, &win)) != FA_OK || empty) return s;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
   DeviceCtx* ctx = nullptr;
   if ((s = device_ctx(&ctx)) != FA_OK) return s;
-  const int BH = B * H;
+  const int BH = B * H, BHkv = B * Hkv;
   CUtensorMap tq, tk, tv;
   if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
-  if ((s = make_tile_map(&tk, k, BH, N, d)) != FA_OK) return s;
-  if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tk, k, BHkv, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tv, v, BHkv, N, d)) != FA_OK) return s;
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.BH = BH;
   a.N = N;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.window = win;
   a.group = BH;  // the forward schedules over all heads at once
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
@@ -215,36 +250,54 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
+                 float* lse, int B, int H, int N, int d, int causal,
+                 float scale, void* stream) {
+  return fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, causal, -1, scale, stream);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   bool empty = false;
   if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
-  return ws_layout(B, H, N, d).total;
+  return ws_layout(B, H, H, N, d).total;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
-                 const float* lse, const void* dout, void* dq, void* dk,
-                 void* dv, void* workspace, size_t workspace_bytes, int B,
-                 int H, int N, int d, int causal, float scale, void* stream) {
+size_t fa_bwd_ext_workspace_size(int B, int H, int Hkv, int N, int d) {
+  bool empty = false;
+  int win = -1;
+  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
+  if (check_ext(H, Hkv, N, -1, &win) != FA_OK) return 0;
+  return ws_layout(B, H, Hkv, N, d).total;
+}
+
+fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N,
+                     int d, int causal, int window, float scale,
+                     void* stream) {
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
-  if (s != FA_OK || empty) return s;
+  if (s != FA_OK) return s;
+  int win = -1;
+  if ((s = check_ext(H, Hkv, N, window, &win)) != FA_OK || empty) return s;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
     return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
       !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(B, H, N, d);
+  const WsLayout w = ws_layout(B, H, Hkv, N, d);
   if (!workspace || !aligned(workspace, 16) || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
   DeviceCtx* ctx = nullptr;
   if ((s = device_ctx(&ctx)) != FA_OK) return s;
-  const int BH = B * H;
+  const int BH = B * H, BHkv = B * Hkv;
   char* ws = static_cast<char*>(workspace);
   CUtensorMap tq, tk, tv, tdo, tdq;
   if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
-  if ((s = make_tile_map(&tk, k, BH, N, d)) != FA_OK) return s;
-  if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tk, k, BHkv, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tv, v, BHkv, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tdo, dout, BH, N, d)) != FA_OK) return s;
   if ((s = make_acc_map(&tdq, ws + w.dq_acc_off, BH, N, d)) != FA_OK) return s;
   fa::BwdArgs a{};
@@ -257,11 +310,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dk_acc = reinterpret_cast<float*>(ws + w.dk_acc_off);
+  a.dv_acc = reinterpret_cast<float*>(ws + w.dv_acc_off);
+  a.hpb = w.hpb;
+  a.nsplit = w.nsplit;
   a.BH = BH;
+  a.BHkv = BHkv;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.window = win;
   a.N = N;
   a.N_pad = (int)align_up((size_t)N, fa::kTile);
-  // Re-read per head: Q and dO (bf16) and the fp32 dQ accumulator.
-  a.group = heads_per_group(BH, (size_t)8 * N * d);
+  // Re-read per block row of the schedule (a key/value head, or one split
+  // of its query heads): Q and dO (bf16) and the fp32 dQ accumulator of its
+  // query heads.
+  a.group = heads_per_group(BHkv * w.nsplit, (size_t)8 * N * d * w.hpb);
   a.scale = scale;
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
@@ -277,6 +340,14 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
     e = cudaEventRecord(g_ev_after_main, st);
   if (e == cudaSuccess) e = fa::launch_bwd_post(a, d, elem_blocks, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk,
+                 void* dv, void* workspace, size_t workspace_bytes, int B,
+                 int H, int N, int d, int causal, float scale, void* stream) {
+  return fa_bwd_ext(q, k, v, o, lse, dout, dq, dk, dv, workspace,
+                    workspace_bytes, B, H, H, N, d, causal, -1, scale, stream);
 }
 
 void fa_bwd_set_phase_events(void* before_main, void* after_main) {
@@ -348,7 +419,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
   if (s != FA_OK || empty) return s;
-  if (ws_layout(B, H, N, d).total > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+  if (ws_layout(B, H, H, N, d).total > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return FA_ERR_CUDA;

@@ -28,6 +28,8 @@
 //   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
 // TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T and then dQ [128,256)
 // dK [256, 256+d)  dV [256+d, 256+2d).
+#include <climits>
+
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -104,6 +106,46 @@ enum : uint32_t {
   kWBwdMisaligned = 0x5A1,
 };
 
+// Row `krow` of dK or dV (key/value head bkv) from the TMEM accumulator at
+// column `tcol` (this thread's lane), times `mul`: rounded to bf16 into `out`,
+// or, when the group's query heads are split over several blocks, added in
+// fp32 into `acc` (vector atomics; rounded later by the post kernel).
+template <int D>
+__device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
+                                            float* acc, int bkv, int krow,
+                                            int N, float mul) {
+  const bool valid = krow < N;
+  const size_t row = (size_t)bkv * N + (valid ? krow : 0);
+#pragma unroll 1
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(tcol + ch * 32, v);
+    tmem_wait_ld();
+    reg_fence32(v);
+    if (!valid) continue;
+    if (acc != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(acc + row * D + ch * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4)
+        atomicAdd(dst + v4, make_float4(__uint_as_float(v[4 * v4]) * mul,
+                                        __uint_as_float(v[4 * v4 + 1]) * mul,
+                                        __uint_as_float(v[4 * v4 + 2]) * mul,
+                                        __uint_as_float(v[4 * v4 + 3]) * mul));
+    } else {
+      uint32_t pkv[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pkv[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul,
+                           __uint_as_float(v[2 * e + 1]) * mul);
+      uint4* dst = reinterpret_cast<uint4*>(out + row * D + ch * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
+                             pkv[4 * v4 + 3]);
+    }
+  }
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -118,15 +160,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto* bars = reinterpret_cast<BwdBars*>(smem + L::kBarOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Blocks resident together share a few heads, so their Q/dO tiles and dQ
-  // accumulator rows stay in L2; causal key tile 0 (the most query tiles)
-  // of each head starts first.
+  // Blocks resident together share a few key/value heads, so their Q/dO
+  // tiles and dQ accumulator rows stay in L2; causal key tile 0 (the most
+  // query tiles) of each head starts first.
+  //
+  // A block owns key tile j of key/value head bkv and visits, for each of the
+  // H / Hkv query heads that read that head, the query tiles whose band
+  // reaches tile j (query i sees key k when k <= i if causal and
+  // |i - k| <= window if a window is set); iteration `it` is query head
+  // it / nq_head of the group and query tile i_lo + it % nq_head.
+  //
+  // With many query heads per key/value head (multi-query attention) one
+  // block per (key/value head, key tile) is too coarse: the group's query
+  // heads are then dealt to nsplit blocks of hpb heads each, whose partial
+  // dK_j, dV_j are summed in fp32 (dk_acc, dv_acc) and rounded afterwards.
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const TileSlot slot = grouped_slot((int)blockIdx.x, n_tiles, a.BH, a.group);
-  const int bh = slot.bh;
+  const TileSlot slot =
+      grouped_slot((int)blockIdx.x, n_tiles, a.BHkv * a.nsplit, a.group);
+  const int bkv = slot.bh / a.nsplit;
+  const int split = slot.bh - bkv * a.nsplit;
   const int j = slot.tile;                        // key tile
-  const int i_begin = CAUSAL ? j : 0;             // first query tile
-  const int nq = n_tiles - i_begin;
+  const int qgroup = a.H / a.Hkv;
+  const int qh0 = (bkv / a.Hkv) * a.H + (bkv % a.Hkv) * qgroup + split * a.hpb;
+  int i_lo, i_hi;
+  {
+    const long long k0 = (long long)j * kTile, k1 = k0 + kTile - 1;
+    i_lo = CAUSAL ? j : ((a.window >= 0 && k0 > a.window)
+                             ? (int)((k0 - a.window) / kTile) : 0);
+    i_hi = n_tiles - 1;
+    if (a.window >= 0) {
+      const long long h = (k1 + a.window) / kTile;
+      if (h < i_hi) i_hi = (int)h;
+    }
+  }
+  const int nq = a.hpb * (i_hi - i_lo + 1);
+  // Walks (query head, query tile) in iteration order without divisions.
+  struct QCursor {
+    int bh, i;
+  };
+  auto q_next = [&](QCursor& c) {
+    if (++c.i > i_hi) {
+      c.i = i_lo;
+      ++c.bh;
+    }
+  };
 
   if (threadIdx.x == 0) {
     uint32_t stop = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
@@ -184,14 +261,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int sb = 0; sb < L::kSub; ++sb) {
         tma_load_3d(k_s + sb * kSubTileBytes, &tm_k, &bars->kv_full, sb * 64,
-                    j * kTile, bh);
+                    j * kTile, bkv);
         tma_load_3d(v_s + sb * kSubTileBytes, &tm_v, &bars->kv_full, sb * 64,
-                    j * kTile, bh);
+                    j * kTile, bkv);
       }
       int q_par[2] = {-1, -1}, do_par = -1;
       bool ok = true;
-      for (int it = 0; it < nq; ++it) {
-        const int i = i_begin + it;
+      QCursor cur{qh0, i_lo};
+      for (int it = 0; it < nq; ++it, q_next(cur)) {
+        const int i = cur.i, bh = cur.bh;
         const int stage = it & 1;
         const uint32_t sp = (uint32_t)((it >> 1) & 1);
         // Q_i, LSE2_i, D_i into Q stage it%2
@@ -335,8 +413,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const float c = a.scale_log2;
     bool ok = run;
-    for (int it = 0; it < nq && ok; ++it) {
-      const int i = i_begin + it;
+    // Band: query q (global) sees key k when dmin <= q - k <= dmax (INT_MIN /
+    // INT_MAX: no bound); a tile pair needs the mask only if its offsets
+    // reach outside [dmin, dmax].  Tile offsets fit in int because
+    // N <= 2^30 and the window is below N.
+    const int win = a.window;
+    const int dmin = CAUSAL ? 0 : (win >= 0 ? -win : INT_MIN);
+    const int dmax = win >= 0 ? win : INT_MAX;
+    QCursor cur{qh0, i_lo};
+    for (int it = 0; it < nq && ok; ++it, q_next(cur)) {
+      const int i = cur.i;
       const int stage = it & 1;
       const uint32_t sp = (uint32_t)((it >> 1) & 1);
       const uint32_t par = (uint32_t)(it & 1);
@@ -352,7 +438,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // half a row of S is live; P half h goes to TMEM columns [32h, 32h+32),
       // over S columns that have already been read.
       uint32_t pk[64];
-      const bool diag = CAUSAL && (i == j);
+      const int off0 = (i - j) * kTile;  // q - k where local q = local k
+      const bool edge = (dmin != INT_MIN && off0 - (kTile - 1) < dmin) ||
+                        (dmax != INT_MAX && off0 + (kTile - 1) > dmax);
+      // Local query index q is visible to key row r when q_lo <= q <= q_hi.
+      int q_lo = 0, q_hi = kTile - 1;
+      if (edge) {
+        const long long base = off0 - r;  // q - k = base + local q
+        if (dmin != INT_MIN)
+          q_lo = (int)max(0ll, min((long long)kTile, dmin - base));
+        if (dmax != INT_MAX)
+          q_hi = (int)max(-1ll, min((long long)kTile - 1, dmax - base));
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t s[64];
@@ -369,14 +466,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float x1 = fmaf(__uint_as_float(s[e + 1]), c, -l4.y);
           float x2 = fmaf(__uint_as_float(s[e + 2]), c, -l4.z);
           float x3 = fmaf(__uint_as_float(s[e + 3]), c, -l4.w);
-          if (diag) {  // query q < key r is masked
-            if (q + 0 < r) x0 = -INFINITY;
-            if (q + 1 < r) x1 = -INFINITY;
-            if (q + 2 < r) x2 = -INFINITY;
-            if (q + 3 < r) x3 = -INFINITY;
-          }
           pk[q / 2] = pack_bf16(ex2(x0), ex2(x1));
           pk[q / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
+        }
+        if (edge) {  // P of queries outside [q_lo, q_hi] is exactly 0
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int q = 64 * h + 2 * k;
+            uint32_t keep = 0xffffffffu;
+            if (q < q_lo || q > q_hi) keep &= 0xffff0000u;
+            if (q + 1 < q_lo || q + 1 > q_hi) keep &= 0x0000ffffu;
+            pk[32 * h + k] &= keep;
+          }
         }
         tmem_st32(tl + 32 * h, pk + 32 * h);
       }
@@ -425,28 +526,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdCmpAcc);
     if (ok) {
       tc_fence_after();
-      const int krow = j * kTile + r;
-      const bool valid = krow < a.N;
-      __nv_bfloat16* out = a.dk + ((size_t)bh * a.N + (valid ? krow : 0)) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tl + 256 + ch * 32, v);
-        tmem_wait_ld();
-        reg_fence32(v);
-        uint32_t pkv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pkv[e] = pack_bf16(__uint_as_float(v[2 * e]) * a.scale,
-                             __uint_as_float(v[2 * e + 1]) * a.scale);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
-                                 pkv[4 * v4 + 3]);
-        }
-      }
+      kv_epilogue<D>(tl + 256, a.dk, a.nsplit > 1 ? a.dk_acc : nullptr, bkv,
+                     j * kTile + r, a.N, a.scale);
     }
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
@@ -462,8 +543,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr int kBoxes = D / 32;
     int g = 0;                                       // boxes staged so far
     bool ok = run;
-    for (int it = 0; it < nq && ok; ++it) {
-      const int i = i_begin + it;
+    QCursor cur{qh0, i_lo};
+    for (int it = 0; it < nq && ok; ++it, q_next(cur)) {
+      const int i = cur.i, bh = cur.bh;
       ok = wait_bar_warp(&bars->dq_full, (uint32_t)(it & 1), wc, kWBwdDqFull);
       if (!ok) break;
       tc_fence_after();
@@ -518,28 +600,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdDqAcc);
     if (ok) {
       tc_fence_after();
-      const int krow = j * kTile + r;
-      const bool valid = krow < a.N;
-      __nv_bfloat16* out = a.dv + ((size_t)bh * a.N + (valid ? krow : 0)) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tl + 256 + D + ch * 32, v);
-        tmem_wait_ld();
-        reg_fence32(v);
-        uint32_t pkv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pkv[e] = pack_bf16(__uint_as_float(v[2 * e]),
-                             __uint_as_float(v[2 * e + 1]));
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
-                                 pkv[4 * v4 + 3]);
-        }
-      }
+      kv_epilogue<D>(tl + 256 + D, a.dv, a.nsplit > 1 ? a.dv_acc : nullptr,
+                     bkv, j * kTile + r, a.N, 1.0f);
     }
   }
 
@@ -609,20 +671,41 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n4;
        idx += (long long)gridDim.x * blockDim.x)
     acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.nsplit > 1) {
+    const long long m4 = (long long)a.BHkv * a.N * D / 4;
+    float4* ak = reinterpret_cast<float4*>(a.dk_acc);
+    float4* av = reinterpret_cast<float4*>(a.dv_acc);
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+         idx < m4; idx += (long long)gridDim.x * blockDim.x) {
+      ak[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+      av[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 }
 
-// dQ = scale * accumulator -> bf16, eight elements per thread per step.
-__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
-  const long long n8 = (long long)a.BH * a.N * d / 8;
-  const float4* acc = reinterpret_cast<const float4*>(a.dq_acc);
-  uint4* out = reinterpret_cast<uint4*>(a.dq);
+// out = mul * acc -> bf16 over n8 groups of eight elements.
+__device__ __forceinline__ void round_rows(const float* acc_f, __nv_bfloat16* out_b,
+                                           long long n8, float mul) {
+  const float4* acc = reinterpret_cast<const float4*>(acc_f);
+  uint4* out = reinterpret_cast<uint4*>(out_b);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
        idx += (long long)gridDim.x * blockDim.x) {
     const float4 x = acc[2 * idx], y = acc[2 * idx + 1];
-    out[idx] = make_uint4(pack_bf16(x.x * a.scale, x.y * a.scale),
-                          pack_bf16(x.z * a.scale, x.w * a.scale),
-                          pack_bf16(y.x * a.scale, y.y * a.scale),
-                          pack_bf16(y.z * a.scale, y.w * a.scale));
+    out[idx] = make_uint4(pack_bf16(x.x * mul, x.y * mul),
+                          pack_bf16(x.z * mul, x.w * mul),
+                          pack_bf16(y.x * mul, y.y * mul),
+                          pack_bf16(y.z * mul, y.w * mul));
+  }
+}
+
+// dQ = scale * accumulator -> bf16, eight elements per thread per step; with
+// split key/value groups also dK and dV (already scaled) -> bf16.
+__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
+  round_rows(a.dq_acc, a.dq, (long long)a.BH * a.N * d / 8, a.scale);
+  if (a.nsplit > 1) {
+    const long long m8 = (long long)a.BHkv * a.N * d / 8;
+    round_rows(a.dk_acc, a.dk, m8, 1.0f);
+    round_rows(a.dv_acc, a.dv, m8, 1.0f);
   }
 }
 
@@ -637,7 +720,7 @@ cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  dim3 grid((unsigned)(a.BH * n_tiles));
+  dim3 grid((unsigned)(a.BHkv * a.nsplit * n_tiles));
   kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }

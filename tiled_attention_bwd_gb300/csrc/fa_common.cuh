@@ -48,9 +48,8 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t where) {
 // Wait for the phase of `bar` with the given parity.  Returns false (and
 // never blocks longer than the time limit) if the wait expired here or the
 // block / grid is already stopping.
-static __device__ __noinline__ bool wait_bar_slow(uint64_t* bar,
-                                                   uint32_t parity,
-                                                   WaitCtl c, uint32_t where) {
+__device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
+                                              const WaitCtl& c, uint32_t where) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
@@ -68,32 +67,56 @@ static __device__ __noinline__ bool wait_bar_slow(uint64_t* bar,
   }
 }
 
+// Out-of-line copy of the polling loop, which keeps the waits of kernels
+// compiled at one register count small.  Kernels that change their register
+// count per warpgroup (setmaxnreg) cannot call functions and use the inline
+// form (kInline = true).
+static __device__ __noinline__ bool wait_bar_slow(uint64_t* bar,
+                                                   uint32_t parity,
+                                                   WaitCtl c, uint32_t where) {
+  return wait_bar_poll(bar, parity, c, where);
+}
+
+template <bool kInline = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
                                          const WaitCtl& c, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, c, where);
+  if constexpr (kInline) return wait_bar_poll(bar, parity, c, where);
+  else return wait_bar_slow(bar, parity, c, where);
 }
 
 // Drain wait used only while a block is stopping: waits for an in-flight copy
 // or MMA (which complete on their own) with a time limit, ignoring the abort
 // flags.  Returns false if even that expired.
-static __device__ __noinline__ bool drain_bar(uint64_t* bar, uint32_t parity,
-                                       uint64_t timeout_ns) {
+__device__ __forceinline__ bool drain_bar_poll(uint64_t* bar, uint32_t parity,
+                                               uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > timeout_ns) return false;
   }
   return true;
 }
+static __device__ __noinline__ bool drain_bar_slow(uint64_t* bar,
+                                                    uint32_t parity,
+                                                    uint64_t timeout_ns) {
+  return drain_bar_poll(bar, parity, timeout_ns);
+}
+template <bool kInline = false>
+__device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity,
+                                          uint64_t timeout_ns) {
+  if constexpr (kInline) return drain_bar_poll(bar, parity, timeout_ns);
+  else return drain_bar_slow(bar, parity, timeout_ns);
+}
 
 // Warp-uniform wait: every lane waits (a single polling lane with the rest
 // parked was measured markedly slower), and the warp proceeds only if all
 // lanes saw the phase complete, so warp-collective tcgen05 loads/stores are
 // never executed by a partial warp.
+template <bool kInline = false>
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity,
                                               const WaitCtl& c,
                                               uint32_t where) {
-  bool ok = wait_bar(bar, parity, c, where);
+  bool ok = wait_bar<kInline>(bar, parity, c, where);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -20,6 +20,13 @@
 // tile's MMAs (ping-pong).  Causal blocks stop at the diagonal tile; only the
 // diagonal (and a ragged last tile) is masked.
 //
+// Two variants the pages list as future work are folded in: grouped /
+// multi-query attention (H query heads share Hkv key/value heads; query
+// head h reads K/V head h / (H / Hkv)) and a sliding window (key j visible
+// to query i only if |i - j| <= window).  A window narrows each Q tile's key
+// tiles to the band and masks the tiles its edges cross; without one (and
+// with Hkv = H) the kernel is the plain operation.
+//
 // TMEM columns (512 allocated): S0, S1 | O0, O1 (see FwdLayout).
 #include "fa_common.cuh"
 #include "fa_launch.h"
@@ -27,9 +34,25 @@
 namespace fa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+// Warps 0-3: softmax for Q tile 0; 4-7: tile 1; 8: TMA producer; 9: MMA
+// issuer.  With kSplitRegs the block has 12 warps (three warpgroups; 10 and
+// 11 idle): launched at kLaunchRegs registers per thread, the control group
+// drops to kCtrlRegs and the softmax groups rise to kSoftmaxRegs, with
+// 2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <= 384 * kLaunchRegs.  Without it
+// the block has 10 warps at 168 registers each (65536 / 320, rounded down to
+// a multiple of 8 and limited by the three warps on two of the four
+// schedulers).
+constexpr bool kSplitRegs = true;
+constexpr int kFwdThreads = kSplitRegs ? 384 : 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kLaunchRegs = 168;
+constexpr bool kInl = kSplitRegs;  // waits inline: no calls under setmaxnreg
+constexpr int kCtrlRegs = 96;
+constexpr int kSoftmaxRegs = 200;
+static_assert(!kSplitRegs || 2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <=
+                                  kFwdThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 
 // Shared memory: two Q tiles and a ring of K/V tiles, all 128 rows.
@@ -105,11 +128,31 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
   }
 }
 
-// One work item = (head, pair of Q tiles).  Causal: pair p needs key tiles
-// 0..2p (first Q tile) and 0..2p+1 (second); the second tile may not exist
-// when the tile count is odd.
+// Key tiles [lo, hi] that Q tile qt must visit.  Query i sees key j when
+// j <= i (causal) and |i - j| <= window (window >= 0); rows and keys past N
+// are handled by the masks.  `window` is below N here (a wider band is the
+// same as none and is passed as -1).
+template <bool CAUSAL>
+__device__ __forceinline__ void key_range(int qt, int n_tiles, int window,
+                                          int& lo, int& hi) {
+  const long long q0 = (long long)qt * kTile, q1 = q0 + kTile - 1;
+  lo = (window >= 0 && q0 > window) ? (int)((q0 - window) / kTile) : 0;
+  if (CAUSAL) {
+    hi = qt;
+  } else if (window >= 0) {
+    const long long h = (q1 + window) / kTile;
+    hi = h < n_tiles - 1 ? (int)h : n_tiles - 1;
+  } else {
+    hi = n_tiles - 1;
+  }
+}
+
+// One work item = (query head, pair of Q tiles).  Tile t visits key tiles
+// lo_t..hi_t; the K/V stream covers jb..je, the union of both ranges (a
+// missing second tile has hi1 = -1).  K/V come from the item's key/value
+// head: query head h of a batch entry reads head h / (H / Hkv).
 struct FwdItem {
-  int bh, qt0, qt1, nkv0, nkv1, nkv;
+  int bh, kvh, qt0, qt1, lo0, hi0, lo1, hi1, jb, je;
 };
 // Items are ordered heaviest first over the whole grid (pair index slow,
 // head fast; causal pairs from the last one down).  Measured: grouping heads
@@ -117,16 +160,24 @@ struct FwdItem {
 // it saved, so the forward uses the global order.
 template <bool CAUSAL>
 __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
-                                            int BH) {
-  const int rank = w / BH;
+                                            const FwdArgs& a) {
+  const int rank = w / a.BH;
   const int pair = CAUSAL ? (n_pairs - 1 - rank) : rank;
   FwdItem it;
-  it.bh = w - rank * BH;
+  it.bh = w - rank * a.BH;
+  const int b = it.bh / a.H, h = it.bh - b * a.H;
+  it.kvh = b * a.Hkv + h / (a.H / a.Hkv);
   it.qt0 = 2 * pair;
   it.qt1 = 2 * pair + 1;
-  it.nkv0 = CAUSAL ? it.qt0 + 1 : n_tiles;
-  it.nkv1 = (it.qt1 < n_tiles) ? (CAUSAL ? it.qt1 + 1 : n_tiles) : 0;
-  it.nkv = it.nkv0 > it.nkv1 ? it.nkv0 : it.nkv1;
+  key_range<CAUSAL>(it.qt0, n_tiles, a.window, it.lo0, it.hi0);
+  if (it.qt1 < n_tiles) {
+    key_range<CAUSAL>(it.qt1, n_tiles, a.window, it.lo1, it.hi1);
+  } else {
+    it.lo1 = 0;
+    it.hi1 = -1;
+  }
+  it.jb = it.lo0;  // lo1 >= lo0
+  it.je = it.hi0 > it.hi1 ? it.hi0 : it.hi1;
   return it;
 }
 
@@ -142,7 +193,7 @@ __device__ __forceinline__ int fwd_round_item(int r) {
 // phases run on across items, so the producer fetches the next item's Q and
 // K/V while the current one finishes, and the next item's first Q K^T
 // overlaps the softmax warps' epilogue.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
@@ -185,6 +236,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{a.st, &bars->abort, a.timeout_ns};
 
+  // Each role's code sits inside the branch that sets its register count,
+  // so that the compiler sizes it for that count.
+  if (kSplitRegs && warp >= 8) reg_dealloc<kCtrlRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && run) {
@@ -200,13 +254,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
            w = fwd_round_item(++r)) {
-        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
+        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (!ok || (t == 1 && itm.nkv1 == 0)) break;
+          if (!ok || (t == 1 && itm.hi1 < 0)) break;
           uint32_t& q_cnt = t ? q_cnt1 : q_cnt0;
           // Q_t must no longer be read by the previous item's Q K^T.
-          ok = wait_bar(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
+          ok = wait_bar<kInl>(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars->q_full[t], L::kTileBytes);
 #pragma unroll
@@ -216,9 +270,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         (t ? itm.qt1 : itm.qt0) * kTile, itm.bh);
           ++q_cnt;
         }
-        for (int j = 0; j < itm.nkv && ok; ++j) {
+        for (int j = itm.jb; j <= itm.je && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv) {  // 0: K_j, 1: V_j
-            ok = wait_bar(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
+            ok = wait_bar<kInl>(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
             if (!ok) break;
             mbar_arrive_expect_tx(&bars->kv_full[stage], L::kTileBytes);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
@@ -226,7 +280,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int sb = 0; sb < L::kSub; ++sb)
               tma_load_3d(smem + L::kKVOff + stage * L::kTileBytes +
                               sb * kSubTileBytes,
-                          m, &bars->kv_full[stage], sb * 64, j * kTile, itm.bh);
+                          m, &bars->kv_full[stage], sb * 64, j * kTile, itm.kvh);
             last_par[stage] = (int)phase;
             if (++stage == S) {
               stage = 0;
@@ -237,11 +291,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) {
         // Stopping: let every copy this thread started land before exit.
-        if (q_cnt0 > 0) drain_bar(&bars->q_full[0], (q_cnt0 - 1) & 1u, a.timeout_ns);
-        if (q_cnt1 > 0) drain_bar(&bars->q_full[1], (q_cnt1 - 1) & 1u, a.timeout_ns);
+        if (q_cnt0 > 0) drain_bar<kInl>(&bars->q_full[0], (q_cnt0 - 1) & 1u, a.timeout_ns);
+        if (q_cnt1 > 0) drain_bar<kInl>(&bars->q_full[1], (q_cnt1 - 1) & 1u, a.timeout_ns);
         for (int s = 0; s < S; ++s)
           if (last_par[s] >= 0)
-            drain_bar(&bars->kv_full[s], (uint32_t)last_par[s], a.timeout_ns);
+            drain_bar<kInl>(&bars->kv_full[s], (uint32_t)last_par[s], a.timeout_ns);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -260,37 +314,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       auto next_kv = [&](int& st) -> bool {
         st = stage;
-        const bool rr = wait_bar(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
+        const bool rr = wait_bar<kInl>(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
         return rr;
       };
-      // Q K^T for tile t and key tile x; after the tile's last one, Q_t is
-      // released to the producer (in-order completion).
-      auto qk = [&](int t, int x, int nkv_t, uint32_t k_a) {
+      // Q K^T for tile t and key tile x; after the tile's last one (hi_t),
+      // Q_t is released to the producer (in-order completion).
+      auto qk = [&](int t, int x, int hi_t, uint32_t k_a) {
         issue_qk<D>(tS(t), q_addr(t), k_a);
         mma_commit(&bars->s_full[t]);
-        if (x == nkv_t - 1) mma_commit(&bars->q_empty[t]);
+        if (x == hi_t) mma_commit(&bars->q_empty[t]);
       };
       for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
            w = fwd_round_item(++r)) {
-        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
-        ok = wait_bar(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
+        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
+        auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
+        auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
+        ok = wait_bar<kInl>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
         ++q_cnt0;
-        if (ok && itm.nkv1 > 0) {
-          ok = wait_bar(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
+        if (ok && itm.hi1 >= 0) {
+          ok = wait_bar<kInl>(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
           ++q_cnt1;
         }
         int k_stage = 0;
         if (ok) ok = next_kv(k_stage);
         if (!ok) break;
         tc_fence_after();
-        qk(0, 0, itm.nkv0, kv_addr + k_stage * L::kTileBytes);
-        if (itm.nkv1 > 0) qk(1, 0, itm.nkv1, kv_addr + k_stage * L::kTileBytes);
+        qk(0, itm.jb, itm.hi0, kv_addr + k_stage * L::kTileBytes);
+        if (act1(itm.jb)) qk(1, itm.jb, itm.hi1, kv_addr + k_stage * L::kTileBytes);
         mma_commit(&bars->kv_empty[k_stage]);
-        for (int j = 0; j < itm.nkv && ok; ++j) {
+        for (int j = itm.jb; j <= itm.je && ok; ++j) {
           int v_stage = 0;
           ok = next_kv(v_stage);
           if (!ok) break;
@@ -298,44 +354,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t v_addr = kv_addr + v_stage * L::kTileBytes;
           int kn_stage = -1;
           // Tile 0: P V for key tile j, then Q K^T for key tile j+1.
-          if (j < itm.nkv0) {
-            ok = wait_bar(&bars->p_full[0], p_cnt0 & 1u, wc, kWFwdMmaP);
+          if (act0(j)) {
+            ok = wait_bar<kInl>(&bars->p_full[0], p_cnt0 & 1u, wc, kWFwdMmaP);
             ++p_cnt0;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<D>(tO(0), tS(0), v_addr, j > 0);
+            issue_pv<D>(tO(0), tS(0), v_addr, j > itm.lo0);
           }
-          if (j + 1 < itm.nkv) {
+          if (j < itm.je) {
             ok = next_kv(kn_stage);
             if (!ok) break;
             tc_fence_after();
           }
-          if (j + 1 < itm.nkv0)
-            qk(0, j + 1, itm.nkv0, kv_addr + kn_stage * L::kTileBytes);
-          else if (j == itm.nkv0 - 1)
+          if (act0(j + 1))
+            qk(0, j + 1, itm.hi0, kv_addr + kn_stage * L::kTileBytes);
+          else if (j == itm.hi0)
             mma_commit(&bars->o_done[0]);
           // Tile 1: the same; V_j is released after both tiles used it.
-          if (j < itm.nkv1) {
-            ok = wait_bar(&bars->p_full[1], p_cnt1 & 1u, wc, kWFwdMmaP);
+          if (act1(j)) {
+            ok = wait_bar<kInl>(&bars->p_full[1], p_cnt1 & 1u, wc, kWFwdMmaP);
             ++p_cnt1;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<D>(tO(1), tS(1), v_addr, j > 0);
+            issue_pv<D>(tO(1), tS(1), v_addr, j > itm.lo1);
           }
           mma_commit(&bars->kv_empty[v_stage]);
-          if (j + 1 < itm.nkv1)
-            qk(1, j + 1, itm.nkv1, kv_addr + kn_stage * L::kTileBytes);
-          else if (j == itm.nkv1 - 1)
+          if (act1(j + 1))
+            qk(1, j + 1, itm.hi1, kv_addr + kn_stage * L::kTileBytes);
+          else if (j == itm.hi1)
             mma_commit(&bars->o_done[1]);
           if (kn_stage >= 0) mma_commit(&bars->kv_empty[kn_stage]);
         }
       }
       // Every MMA issued above must finish before TMEM is released.
       mma_commit(&bars->mma_done);
-      drain_bar(&bars->mma_done, 0, a.timeout_ns);
+      drain_bar<kInl>(&bars->mma_done, 0, a.timeout_ns);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------- softmax (thread = row)
+    if constexpr (kSplitRegs) reg_alloc<kSoftmaxRegs>();
     const int t = warp >> 2, quarter = warp & 3;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = tl + t * 128;
@@ -345,13 +402,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = run;
     for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
          w = fwd_round_item(++r)) {
-      const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a.BH);
-      const int nkv_t = t ? itm.nkv1 : itm.nkv0;
-      if (nkv_t == 0) continue;
-      const int qrow = (t ? itm.qt1 : itm.qt0) * kTile + quarter * 32 + lane;
+      const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
+      const int lo_t = t ? itm.lo1 : itm.lo0;
+      const int hi_t = t ? itm.hi1 : itm.hi0;
+      if (hi_t < 0) continue;
+      const int q0 = (t ? itm.qt1 : itm.qt0) * kTile;
+      const int qrow = q0 + quarter * 32 + lane;
+      // Visible keys of a row: j <= i (causal), |i - j| <= window, j < N.
+      // Without a window only the last key tile can need the mask (the
+      // diagonal, or keys past a ragged N).  With one, a key tile needs it
+      // if it reaches below the Q tile's largest lower bound or above its
+      // smallest upper bound; the window is below N, so none of these sums
+      // overflows.
+      const int win = a.window, nm1 = a.N - 1;
+      const int klo_max = WINDOW ? q0 + kTile - 1 - win : -1;
+      const int khi_min =
+          CAUSAL ? q0 : (WINDOW ? (q0 > nm1 - win ? nm1 : q0 + win) : nm1);
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv_t; ++j) {
-        ok = wait_bar_warp(&bars->s_full[t], s_cnt & 1u, wc, kWFwdSmS);
+      for (int j = lo_t; j <= hi_t; ++j) {
+        ok = wait_bar_warp<kInl>(&bars->s_full[t], s_cnt & 1u, wc, kWFwdSmS);
         ++s_cnt;
         if (!ok) break;
         tc_fence_after();
@@ -365,23 +434,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         reg_fence32(s + 32);
         reg_fence32(s + 64);
         reg_fence32(s + 96);
-        // Mask: the diagonal tile (causal) or keys past N (ragged last tile).
-        if ((j == nkv_t - 1) && (CAUSAL || (a.N & (kTile - 1)))) {
-          const int lim = (CAUSAL ? qrow : a.N - 1) - j * kTile;
+        if constexpr (!WINDOW) {
+          if (j == hi_t && (CAUSAL || (a.N & (kTile - 1)))) {
+            const int lim = (CAUSAL ? qrow : nm1) - j * kTile;
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e > lim) s[e] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 128; ++e)
+              if (e > lim) s[e] = __float_as_uint(-INFINITY);
+          }
+        } else {
+          const int kb = j * kTile;
+          if (kb < klo_max || kb + kTile - 1 > khi_min) {
+            const int row_lo = qrow > win ? qrow - win : 0;
+            const int row_hi =
+                CAUSAL ? qrow : (qrow > nm1 - win ? nm1 : qrow + win);
+            const int e_lo = row_lo - kb, e_hi = row_hi - kb;
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if (e < e_lo || e > e_hi) s[e] = __float_as_uint(-INFINITY);
+          }
         }
-        // Row max as eight independent chains (a single chain of 128
-        // dependent max operations dominated the softmax latency).
-        float mx8[8];
+        // Row max: four independent chains of three-input maxima (one long
+        // dependent chain dominated the softmax latency).
+        float mx4[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(s[k]);
+        for (int k = 0; k < 4; ++k)
+          mx4[k] = fmaxf(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
 #pragma unroll
-        for (int e = 8; e < 128; ++e)
-          mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(s[e]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int e = 8; e < 128; e += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mx4[k] = max3(mx4[k], __uint_as_float(s[e + 2 * k]),
+                          __uint_as_float(s[e + 2 * k + 1]));
+        const float mx = max3(max3(mx4[0], mx4[1], mx4[2]), mx4[3], mx4[3]);
         const float m_tile = mx * c;
         // Lazy rescale: keep the reference max until the row max exceeds it
         // by more than the threshold; exp2(x - m_ref) <= 2^8 meanwhile.
@@ -392,24 +476,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_ref = m_tile;
         }
         l *= alpha;
-        const float neg_m = -m_ref;
-        float l8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
-        // P is packed in place: pair (e, e+1) goes to s[e/2], a slot whose
-        // score has already been consumed, so no second array is live.
+        // With a window a row may have seen no visible key yet (m_ref =
+        // -inf): its P is 0, not exp2(-inf + inf).
+        float neg_m = -m_ref;
+        if constexpr (WINDOW) neg_m = (m_ref == -INFINITY) ? 0.f : neg_m;
+        const uint64_t c2 = bcast2(c), nm2 = bcast2(neg_m);
+        // Scores to exponents two at a time (packed fp32 FMA), row sum in
+        // four packed partial sums; P is packed in place: pair (e, e+1) goes
+        // to s[e/2], a slot whose score has already been consumed.
+        float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 128; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[e + 0]), c, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), c, neg_m));
-          l8[e & 7] += p0;
-          l8[(e + 1) & 7] += p1;
+          float x0, x1;
+          fma2_bcast(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]),
+                     c2, nm2);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          add2_acc(la[(e >> 1) & 3], lb[(e >> 1) & 3], p0, p1);
           s[e / 2] = pack_bf16(p0, p1);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
         tmem_st32(tS + 0, s);
         tmem_st32(tS + 32, s + 32);
-        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        if (j > lo_t && __any_sync(0xffffffffu, bump)) {
           // Rescale O_t, which holds P V for tiles < j (the S_t(j) commit
           // came after them); done after P is stored so that the scores are
           // no longer live.  P V for tile j waits for p_full below.
@@ -430,7 +518,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         warp_arrive(&bars->p_full[t]);
       }
       if (!ok) break;
-      ok = wait_bar_warp(&bars->o_done[t], o_cnt & 1u, wc, kWFwdSmO);
+      ok = wait_bar_warp<kInl>(&bars->o_done[t], o_cnt & 1u, wc, kWFwdSmO);
       ++o_cnt;
       if (!ok) break;
       tc_fence_after();
@@ -472,14 +560,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  auto kern = fwd_kernel<D, CAUSAL, WINDOW>;
+  cudaError_t e;
+  if constexpr (kSplitRegs) {
+    // The register split inside the kernel assumes exactly kLaunchRegs per
+    // thread at launch; with fewer the softmax groups' setmaxnreg.inc could
+    // never be granted, so such a build is refused here.
+    cudaFuncAttributes fa_attr{};
+    e = cudaFuncGetAttributes(&fa_attr, kern);
+    if (e != cudaSuccess) return e;
+    if (fa_attr.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int n_items = BH * ((n_tiles + 1) / 2);
@@ -488,16 +586,25 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   return cudaGetLastError();
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_w(const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const FwdArgs& a, int BH,
+                         int grid_blocks, cudaStream_t stream) {
+  return a.window >= 0
+             ? launch_fwd_t<D, CAUSAL, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+             : launch_fwd_t<D, CAUSAL, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
                        bool causal, int grid_blocks, cudaStream_t stream) {
   if (d == 128)
-    return causal ? launch_fwd_t<128, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                  : launch_fwd_t<128, false>(tq, tk, tv, a, BH, grid_blocks, stream);
-  return causal ? launch_fwd_t<64, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                : launch_fwd_t<64, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+    return causal ? launch_fwd_w<128, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                  : launch_fwd_w<128, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+  return causal ? launch_fwd_w<64, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                : launch_fwd_w<64, false>(tq, tk, tv, a, BH, grid_blocks, stream);
 }
 
 }  // namespace fa

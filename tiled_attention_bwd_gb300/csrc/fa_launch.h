@@ -13,8 +13,11 @@ struct DevState;
 struct FwdArgs {
   __nv_bfloat16* o;     // [BH, N, d]
   float* lse;           // [BH, N]
-  int BH;
+  int BH;               // batch x query heads
   int N;
+  int H;                // query heads per batch entry
+  int Hkv;              // key/value heads per batch entry (divides H)
+  int window;           // band half-width in keys, < 0: none
   int group;            // heads per scheduling group
   float scale_log2;     // scale * log2(e): scores enter exp2 directly
   DevState* st;
@@ -29,12 +32,20 @@ struct BwdArgs {
   float* ddot;                // [BH, N_pad] D_i = dO_i . O_i  (0 past N)
   float* lse2;                // [BH, N_pad] LSE_i * log2(e)   (+inf past N)
   __nv_bfloat16* dq;          // [BH, N, d]
-  __nv_bfloat16* dk;          // [BH, N, d]
-  __nv_bfloat16* dv;          // [BH, N, d]
-  int BH;
+  __nv_bfloat16* dk;          // [BHkv, N, d]
+  __nv_bfloat16* dv;          // [BHkv, N, d]
+  float* dk_acc;              // [BHkv, N, d] fp32, used when nsplit > 1
+  float* dv_acc;              // [BHkv, N, d] fp32, used when nsplit > 1
+  int BH;                     // batch x query heads
+  int BHkv;                   // batch x key/value heads
+  int H;                      // query heads per batch entry
+  int Hkv;                    // key/value heads per batch entry (divides H)
+  int window;                 // band half-width in keys, < 0: none
+  int hpb;                    // query heads per block (divides H / Hkv)
+  int nsplit;                 // blocks per (key/value head, key tile)
   int N;
   int N_pad;                  // N rounded up to a multiple of 128
-  int group;                  // heads per scheduling group
+  int group;                  // key/value heads per scheduling group
   float scale;
   float scale_log2;
   DevState* st;

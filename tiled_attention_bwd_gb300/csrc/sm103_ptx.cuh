@@ -258,6 +258,21 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ------------------------------------------------------------ arithmetic
 // Hardware base-2 exponential / logarithm (MUFU.EX2 / MUFU.LG2).
+// Warpgroup register reallocation: every warp of a warpgroup executes the
+// same call.  .dec returns registers to the block's pool; .inc waits until
+// the pool holds enough, so the shares of all warpgroups must add up to at
+// most the registers the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -269,6 +284,39 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
+// Packed pairs of fp32 (one instruction for two lanes' worth of work):
+// (d0, d1) = (a0, a1) * (b, b) + (c, c).
+__device__ __forceinline__ void fma2_bcast(float& d0, float& d1, float a0,
+                                           float a1, uint64_t b2, uint64_t c2) {
+  asm("{\n\t.reg .b64 t;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "fma.rn.f32x2 t, t, %4, %5;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b2), "l"(c2));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void add2_acc(float& d0, float& d1, float a0,
+                                         float a1) {
+  asm("{\n\t.reg .b64 t, u;\n\t"
+      "mov.b64 t, {%0, %1};\n\t"
+      "mov.b64 u, {%2, %3};\n\t"
+      "add.rn.f32x2 t, t, u;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+// Both halves of a packed pair set to x.
+__device__ __forceinline__ uint64_t bcast2(float x) {
+  return ((uint64_t)__float_as_uint(x) << 32) | __float_as_uint(x);
+}
+// Three-input maximum.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

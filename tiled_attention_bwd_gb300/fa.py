@@ -61,6 +61,13 @@ def open_library(path: str):
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                            ctypes.c_size_t, i, i, i, i, i, f, vp]
     lib.fa_bwd.restype = i
+    lib.fa_fwd_ext.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_ext.restype = i
+    lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                               ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
+    lib.fa_bwd_ext.restype = i
+    lib.fa_bwd_ext_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_ext_workspace_size.restype = ctypes.c_size_t
     lib.fa_check_device_status.argtypes = [vp]
     lib.fa_check_device_status.restype = i
     lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -193,6 +200,86 @@ def fa_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None,
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
             workspace.numel() * workspace.element_size(), B, H, N, d,
             int(bool(causal)), float(scale), _stream_handle(q.device)))
+    return dq, dk, dv
+
+
+def fa_bwd_ext_workspace_size(B: int, H: int, Hkv: int, N: int,
+                              d: int) -> int:
+    return int(load_library().fa_bwd_ext_workspace_size(B, H, Hkv, N, d))
+
+
+def _check_ext_shapes(q, k):
+    """[B,H,N,d] queries, [B,Hkv,N,d] keys/values with Hkv dividing H
+    (shapes only; dtype, device and layout are checked by _check_qkv)."""
+    for name, t in (("q", q), ("k", k)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError("%s must be a 4-D tensor" % name)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, N, d) or Hkv < 1 or H % Hkv != 0:
+        raise ValueError("k has shape %s; expected [B,Hkv,N,d] = [%d,Hkv,%d,%d]"
+                         " with Hkv dividing H = %d" % (tuple(k.shape), B, N,
+                                                        d, H))
+    return B, H, Hkv, N, d
+
+
+def fa_fwd_ext(q, k, v, causal: bool, scale: float, window: int = -1,
+               out=None, lse=None):
+    """Forward pass with Hkv = k.shape[1] key/value heads shared by the
+    query heads (grouped / multi-query attention) and an optional sliding
+    window (|i - j| <= window; < 0: none).  Returns (O, LSE)."""
+    lib = load_library()
+    B, H, Hkv, N, d = _check_ext_shapes(q, k)
+    _check_qkv("q", q)
+    _check_qkv("k", k, (B, Hkv, N, d))
+    _check_qkv("v", v, (B, Hkv, N, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _check_qkv("out", out, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    with torch.cuda.device(q.device):
+        _check("fa_fwd_ext", lib.fa_fwd_ext(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+            int(bool(causal)), int(window), float(scale),
+            _stream_handle(q.device)))
+    return out, lse
+
+
+def fa_bwd_ext(q, k, v, o, lse, dout, causal: bool, scale: float,
+               window: int = -1, dq=None, dk=None, dv=None, workspace=None):
+    """Backward of fa_fwd_ext.  Returns (dQ [B,H,N,d], dK, dV [B,Hkv,N,d]);
+    dK and dV are summed over the query heads sharing each K/V head."""
+    lib = load_library()
+    B, H, Hkv, N, d = _check_ext_shapes(q, k)
+    _check_qkv("q", q)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    for name, t in (("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_qkv("dq", dq, q.shape)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    need = fa_bwd_ext_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=q.device)
+    with torch.cuda.device(q.device):
+        _check("fa_bwd_ext", lib.fa_bwd_ext(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+            int(bool(causal)), int(window), float(scale),
+            _stream_handle(q.device)))
     return dq, dk, dv
 
 

@@ -85,6 +85,41 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int,
     return out
 
 
+def make_grouped_inputs(B: int, H: int, Hkv: int, N: int, d: int, seed: int,
+                        qk_mult: float = 1.0):
+    """Inputs with Hkv key/value heads: q, do [B,H,N,d]; k, v [B,Hkv,N,d]
+    (same recipe, drawn in the order q, k, v, do)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    for name in ("q", "k", "v", "do"):
+        shape = (B, Hkv if name in ("k", "v") else H, N, d)
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if name in ("q", "k") and qk_mult != 1.0:
+            x.mul_(qk_mult)
+        out[name] = x.to(torch.bfloat16).contiguous()
+        del x
+    return out
+
+
+def visible_pairs(N: int, causal: bool, window: int, r0: int = 0,
+                  r1: int = None) -> int:
+    """Number of (query, key) pairs with the query in rows [r0, r1) that a
+    query/key length N leaves visible: key j is visible to query i when
+    j <= i (causal) and |i - j| <= window (window >= 0).  Used only to count
+    the work a band does."""
+    r1 = N if r1 is None else r1
+    i = np.arange(r0, r1, dtype=np.int64)
+    lo = np.maximum(0, i - window) if window >= 0 else np.zeros_like(i)
+    if causal:
+        hi = i
+    elif window >= 0:
+        hi = np.minimum(N - 1, i + window)
+    else:
+        hi = np.full_like(i, N - 1)
+    return int((hi - lo + 1).sum())
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
 
@@ -103,4 +138,5 @@ def sample_heads(n_heads: int, count: int, seed: int):
 
 
 __all__ = ["Workload", "WORKLOADS", "HEADLINE", "default_scale", "make_inputs",
-           "workload_inputs", "sample_heads"]
+           "make_grouped_inputs", "visible_pairs", "workload_inputs",
+           "sample_heads"]
