@@ -310,12 +310,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_st = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, D, true, true);
-      const uint32_t k_a = smem_addr(k_s), v_a = smem_addr(v_s);
-      const uint32_t do_a = smem_addr(do_s), ds_a = smem_addr(ds_s);
       const uint32_t tS = tmem, tDP = tmem + 128;
       const uint32_t tDK = tmem + 256, tDV = tmem + 256 + D;
-      auto q_addr = [&](int it) {
-        return smem_addr(smem + L::kQOff + (it & 1) * L::kQStageBytes);
+      // Operand descriptors, fixed for the block's lifetime (K-major: 16-wide
+      // K steps 32 bytes apart within 128-byte rows, sub-tiles 16 KB apart;
+      // MN-major: 16-row K steps 2048 bytes apart).
+      const uint64_t k_km = sdesc_sw128(smem_addr(k_s), 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_addr(k_s), kSubTileBytes, 1024);
+      const uint64_t v_km = sdesc_sw128(smem_addr(v_s), 16, 1024);
+      const uint64_t do_km = sdesc_sw128(smem_addr(do_s), 16, 1024);
+      const uint64_t do_mn = sdesc_sw128(smem_addr(do_s), kSubTileBytes, 1024);
+      const uint64_t ds_km = sdesc_sw128(smem_addr(ds_s), 16, 1024);
+      const uint64_t ds_mn = sdesc_sw128(smem_addr(ds_s), kSubTileBytes, 1024);
+      const uint64_t q_km0 = sdesc_sw128(smem_addr(smem + L::kQOff), 16, 1024);
+      const uint64_t q_mn0 =
+          sdesc_sw128(smem_addr(smem + L::kQOff), kSubTileBytes, 1024);
+      auto q_km = [&](int it) { return sdesc_adv(q_km0, (it & 1) * L::kQStageBytes); };
+      auto q_mn = [&](int it) { return sdesc_adv(q_mn0, (it & 1) * L::kQStageBytes); };
+      auto kstep = [](int s) {  // K-major offset of 16-wide K step s
+        return (uint32_t)((s >> 2) * kSubTileBytes + (s & 3) * 32);
       };
       // Software pipeline: S^T and dP^T of tile it+1 are issued around the
       // dK/dQ MMAs of tile it, so the P/dS warps work on tile it+1 while the
@@ -324,22 +337,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // S^T(it+1) may overwrite P^T(it) because dV(it) precedes it in the
       // tensor core's in-order queue.
       auto issue_st = [&](int it) {  // S^T = K_j Q_i^T  [keys x queries]
-        const uint32_t q_a = q_addr(it);
+        const uint64_t qd = q_km(it);
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
-          const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
-          mma_ss(tS, sdesc_sw128(k_a + off, 16, 1024),
-                 sdesc_sw128(q_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
-        }
+        for (int s = 0; s < D / 16; ++s)
+          mma_ss(tS, sdesc_adv(k_km, kstep(s)), sdesc_adv(qd, kstep(s)), id_st,
+                 s > 0 ? 1u : 0u);
         mma_commit(&bars->s_full);
       };
       auto issue_dp = [&]() {  // dP^T = V_j dO_i^T  [keys x queries]
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
-          const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
-          mma_ss(tDP, sdesc_sw128(v_a + off, 16, 1024),
-                 sdesc_sw128(do_a + off, 16, 1024), id_st, s > 0 ? 1u : 0u);
-        }
+        for (int s = 0; s < D / 16; ++s)
+          mma_ss(tDP, sdesc_adv(v_km, kstep(s)), sdesc_adv(do_km, kstep(s)),
+                 id_st, s > 0 ? 1u : 0u);
         mma_commit(&bars->dp_full);
       };
       bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
@@ -355,15 +364,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       for (int it = 0; it < nq && ok; ++it) {
         const uint32_t par = (uint32_t)(it & 1);
-        const uint32_t q_a = q_addr(it);
         ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
         if (!ok) break;
         tc_fence_after();
         // dV_j += P^T dO_i   [keys x d], K = queries; P^T from TMEM
 #pragma unroll
         for (int s = 0; s < kTile / 16; ++s)
-          mma_ts(tDV, tS + s * 8,
-                 sdesc_sw128(do_a + s * 2048, kSubTileBytes, 1024), id_kv,
+          mma_ts(tDV, tS + s * 8, sdesc_adv(do_mn, s * 2048), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bars->do_empty);   // dO_i no longer needed
         if (it + 1 < nq) {
@@ -377,19 +384,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         tc_fence_after();
         // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T K-major in smem
+        const uint64_t qmn = q_mn(it);
 #pragma unroll
         for (int s = 0; s < kTile / 16; ++s)
-          mma_ss(tDK,
-                 sdesc_sw128(ds_a + (s >> 2) * kSubTileBytes + (s & 3) * 32, 16,
-                             1024),
-                 sdesc_sw128(q_a + s * 2048, kSubTileBytes, 1024), id_kv,
+          mma_ss(tDK, sdesc_adv(ds_km, kstep(s)), sdesc_adv(qmn, s * 2048), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bars->q_empty[it & 1]);   // Q_i, LSE2_i, D_i released
         // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
 #pragma unroll
         for (int s = 0; s < kTile / 16; ++s)
-          mma_ss(tDP, sdesc_sw128(ds_a + s * 2048, kSubTileBytes, 1024),
-                 sdesc_sw128(k_a + s * 2048, kSubTileBytes, 1024), id_q,
+          mma_ss(tDP, sdesc_adv(ds_mn, s * 2048), sdesc_adv(k_mn, s * 2048), id_q,
                  s > 0 ? 1u : 0u);
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free);    // dS_i no longer read

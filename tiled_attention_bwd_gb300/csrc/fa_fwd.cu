@@ -101,29 +101,31 @@ enum : uint32_t {
   kWFwdSmO = 0x302,
 };
 
-// S_t = Q_t K^T: M = N = 128, K = d; both operands K-major in smem.
+// S_t = Q_t K^T: M = N = 128, K = d; both operands K-major in smem.  The
+// descriptors are those of the tiles' first bytes; each 16-wide K step is
+// 32 bytes further along the 128-byte rows, each 64-column sub-tile 16 KB.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr,
-                                         uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc,
+                                         uint64_t k_desc) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
     const uint32_t off = (s >> 2) * kSubTileBytes + (s & 3) * 32;
-    mma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024),
-           sdesc_sw128(k_addr + off, 16, 1024), id, s > 0 ? 1u : 0u);
+    mma_ss(s_tmem, sdesc_adv(q_desc, off), sdesc_adv(k_desc, off), id,
+           s > 0 ? 1u : 0u);
   }
 }
 
 // O_t (+)= P_t V: M = 128, N = d, K = 128 keys; A = P from TMEM, B = V
-// read MN-major (d contiguous in smem).
+// read MN-major (d contiguous in smem; 16 keys = 2048 bytes per K step).
+// v_desc: MN-major descriptor of V's first byte.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
-                                         uint32_t v_addr, bool accumulate) {
+                                         uint64_t v_desc, bool accumulate) {
   constexpr uint32_t id = idesc_bf16(128, D, false, true);
 #pragma unroll
   for (int s = 0; s < kTile / 16; ++s) {
-    mma_ts(o_tmem, p_tmem + s * 8,
-           sdesc_sw128(v_addr + s * 2048, kSubTileBytes, 1024), id,
+    mma_ts(o_tmem, p_tmem + s * 8, sdesc_adv(v_desc, s * 2048), id,
            (accumulate || s > 0) ? 1u : 0u);
   }
 }
@@ -305,7 +307,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // this thread's state lives in local memory.
       const uint32_t q_base = smem_addr(smem + L::kQOff);
       const uint32_t kv_addr = smem_addr(smem + L::kKVOff);
-      auto q_addr = [&](int t) { return q_base + (uint32_t)(t * L::kTileBytes); };
+      // Descriptors of every operand tile, fixed for the kernel's lifetime:
+      // Q_t K-major; ring stage st read K-major (as K) or MN-major (as V).
+      const uint64_t q_desc0 = sdesc_sw128(q_base, 16, 1024);
+      const uint64_t kv_desc_k = sdesc_sw128(kv_addr, 16, 1024);
+      const uint64_t kv_desc_v = sdesc_sw128(kv_addr, kSubTileBytes, 1024);
+      auto q_desc = [&](int t) { return sdesc_adv(q_desc0, t * L::kTileBytes); };
+      auto k_desc = [&](int st) { return sdesc_adv(kv_desc_k, st * L::kTileBytes); };
+      auto v_desc = [&](int st) { return sdesc_adv(kv_desc_v, st * L::kTileBytes); };
       auto tS = [&](int t) { return tmem + (uint32_t)(t * 128); };
       auto tO = [&](int t) { return tmem + (uint32_t)(256 + t * D); };
       int stage = 0;
@@ -323,8 +332,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       // Q K^T for tile t and key tile x; after the tile's last one (hi_t),
       // Q_t is released to the producer (in-order completion).
-      auto qk = [&](int t, int x, int hi_t, uint32_t k_a) {
-        issue_qk<D>(tS(t), q_addr(t), k_a);
+      auto qk = [&](int t, int x, int hi_t, int k_st) {
+        issue_qk<D>(tS(t), q_desc(t), k_desc(k_st));
         mma_commit(&bars->s_full[t]);
         if (x == hi_t) mma_commit(&bars->q_empty[t]);
       };
@@ -343,15 +352,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) ok = next_kv(k_stage);
         if (!ok) break;
         tc_fence_after();
-        qk(0, itm.jb, itm.hi0, kv_addr + k_stage * L::kTileBytes);
-        if (act1(itm.jb)) qk(1, itm.jb, itm.hi1, kv_addr + k_stage * L::kTileBytes);
+        qk(0, itm.jb, itm.hi0, k_stage);
+        if (act1(itm.jb)) qk(1, itm.jb, itm.hi1, k_stage);
         mma_commit(&bars->kv_empty[k_stage]);
         for (int j = itm.jb; j <= itm.je && ok; ++j) {
           int v_stage = 0;
           ok = next_kv(v_stage);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v_addr = kv_addr + v_stage * L::kTileBytes;
+          const uint64_t vd = v_desc(v_stage);
           int kn_stage = -1;
           // Tile 0: P V for key tile j, then Q K^T for key tile j+1.
           if (act0(j)) {
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++p_cnt0;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<D>(tO(0), tS(0), v_addr, j > itm.lo0);
+            issue_pv<D>(tO(0), tS(0), vd, j > itm.lo0);
           }
           if (j < itm.je) {
             ok = next_kv(kn_stage);
@@ -367,7 +376,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tc_fence_after();
           }
           if (act0(j + 1))
-            qk(0, j + 1, itm.hi0, kv_addr + kn_stage * L::kTileBytes);
+            qk(0, j + 1, itm.hi0, kn_stage);
           else if (j == itm.hi0)
             mma_commit(&bars->o_done[0]);
           // Tile 1: the same; V_j is released after both tiles used it.
@@ -376,11 +385,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++p_cnt1;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<D>(tO(1), tS(1), v_addr, j > itm.lo1);
+            issue_pv<D>(tO(1), tS(1), vd, j > itm.lo1);
           }
           mma_commit(&bars->kv_empty[v_stage]);
           if (act1(j + 1))
-            qk(1, j + 1, itm.hi1, kv_addr + kn_stage * L::kTileBytes);
+            qk(1, j + 1, itm.hi1, kn_stage);
           else if (j == itm.hi1)
             mma_commit(&bars->o_done[1]);
           if (kn_stage >= 0) mma_commit(&bars->kv_empty[kn_stage]);

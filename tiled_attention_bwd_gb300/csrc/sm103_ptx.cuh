@@ -170,6 +170,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
+// The descriptor of the operand `byte_off` bytes further on: the start
+// address field holds address / 16 in its low 14 bits, and every shared
+// memory address (below 228 KB) fits there without a carry.
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
                                        uint64_t b_desc, uint32_t idesc,
