@@ -26,6 +26,10 @@ What each function follows:
                  |i - j| <= window, and j <= i when causal).  The pages list
                  both as future variants ("Advanced Features (Future)":
                  multi-query / grouped query attention; sliding window).
+  fp8         -- (submodule) E4M3 quantisation of Q and K per 16-row block
+                 with one float32 scale each, and the forward on the
+                 dequantised values ("GPU Performance Optimization Batch 1 --
+                 Design Spec", Item 3, "Optional FP8 path").
   bwd         -- gradients dQ, dK, dV of L with dL/dO = dout, P recomputed
                  from the row's LSE ("GPU Performance Optimization Batch 1 --
                  Design Spec", Item 3, backward paragraph).  The formulas come
