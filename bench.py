@@ -1,7 +1,7 @@
 """Benchmark: attention forward + backward TFLOP/s on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--hkv HKV] [--window W]
+                    [--hkv HKV] [--window W] [--fp8]
                     [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
 
 One step = fa_fwd + fa_bwd over the whole workload (default: 4x64x4096x128
@@ -322,6 +322,31 @@ def run_ours(args, w, rank, world, local):
     torch.cuda.synchronize(dev)
     fwd_ms = max_over_ranks(fw_s.elapsed_time(fw_e) / K, world, dev)
 
+    # -------- FP8 forward (optional): Q, K quantised to E4M3 inside the call
+    fp8 = None
+    if args.fp8:
+        from tiled_attention_bwd_gb300 import fa_fwd_fp8, fa_fwd_fp8_workspace_size
+        ws8 = torch.empty(fa_fwd_fp8_workspace_size(w.B, w.H, w.N, w.d),
+                          dtype=torch.uint8, device=dev)
+        for _ in range(max(3, args.warmup)):
+            fa_fwd_fp8(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws8)
+        torch.cuda.synchronize(dev)
+        f8_s = torch.cuda.Event(enable_timing=True)
+        f8_e = torch.cuda.Event(enable_timing=True)
+        f8_s.record(stream)
+        for _ in range(K):
+            fa_fwd_fp8(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws8)
+        f8_e.record(stream)
+        torch.cuda.synchronize(dev)
+        if fa_check_device_status(dev) != 0:
+            raise RuntimeError("device status error in the FP8 forward")
+        f8_ms = max_over_ranks(f8_s.elapsed_time(f8_e) / K, world, dev)
+        fp8 = {"value": world * fwd_flops / (f8_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "ms": f8_ms,
+               "note": "fa_fwd_fp8: E4M3 quantisation of Q and K (two "
+                       "launches) + forward with Q K^T on FP8 tensor cores; "
+                       "same FLOP convention as fwd"}
+
     # -------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -330,13 +355,32 @@ def run_ours(args, w, rank, world, local):
                 for n in ("o", "dq", "dk", "dv")}
         lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
 
-        def e2e_step():
-            for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
-                t.copy_(host[n], non_blocking=True)
-            step()
-            for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-                outs[n].copy_(t, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+        if variant_config(w, args):
+            # grouped heads / window: copies and compute one after another
+            mode = "serial copies around fa_fwd_ext + fa_bwd_ext"
+
+            def e2e_step():
+                for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+                    t.copy_(host[n], non_blocking=True)
+                step()
+                for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+                    outs[n].copy_(t, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+        else:
+            # fa_step_host: chunks of heads, copies in both directions
+            # overlapped with each other and with the kernels
+            from tiled_attention_bwd_gb300 import (fa_step_host,
+                                                   fa_step_host_scratch_size)
+            mode = "fa_step_host (pinned host buffers, pipelined by head chunks)"
+            scratch = torch.empty(
+                fa_step_host_scratch_size(w.B, w.H, w.N, w.d, args.chunk_heads),
+                dtype=torch.uint8, device=dev)
+
+            def e2e_step():
+                fa_step_host(host["q"], host["k"], host["v"], host["do"],
+                             w.causal, w.scale, outs["o"], lse_h, outs["dq"],
+                             outs["dk"], outs["dv"], scratch=scratch,
+                             chunk_heads=args.chunk_heads, device=dev)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -356,7 +400,8 @@ def run_ours(args, w, rank, world, local):
                + lse_h.numel() * 4)
         e2e = {"value": world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "mode": mode}
 
     traffic = committed_traffic("bwd_main_kernel")
     traffic_bytes = (traffic[0] if traffic and traffic[1] == w.name
@@ -405,6 +450,7 @@ def run_ours(args, w, rank, world, local):
                      "algorithmic_flop_per_launch": bwd_flops},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "fwd_fp8": fp8,
         "gpu_launches": 4 * K,
         "clocks": clocks,
     }
@@ -422,6 +468,10 @@ def main():
                     help="key/value heads (divides H; default H)")
     ap.add_argument("--window", type=int, default=-1,
                     help="sliding window |i - j| <= W (default: none)")
+    ap.add_argument("--chunk-heads", type=int, default=0,
+                    help="heads per chunk of the host-buffer step (0: B*H/16)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="also time the FP8 forward (fa_fwd_fp8)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

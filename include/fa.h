@@ -143,6 +143,66 @@ fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
                      void* stream);
 
 /*
+ * FP8 forward: the optional FP8 path of "GPU Performance Optimization Batch
+ * 1 -- Design Spec", Item 3 ("FlashAttention-3 Blackwell"): before the
+ * Q K^T product, Q and K are quantised to E4M3 block by block, each block
+ * with its own scale, and the product runs on the FP8 tensor cores.
+ *   - Blocks are 16 rows by the whole head dimension of one head:
+ *     scale = amax / 448 in float32 (1 for an all-zero block), code = E4M3
+ *     round-to-nearest-even of x / scale (IEEE float32 division), saturating
+ *     at +-448.  A block spans the head dimension because a scale that
+ *     varied along the contraction could not be applied after the product.
+ *   - S = (Q8 K8^T) * sq_i * sk_j is accumulated in fp32; softmax, P (bf16)
+ *     and O = P V (bf16 V) are as in fa_fwd.  Results therefore differ from
+ *     fa_fwd by the quantisation of Q and K.
+ *   - Same arguments as fa_fwd plus a workspace of
+ *     fa_fwd_fp8_workspace_size(B, H, N, d) bytes (E4M3 copies of Q and K
+ *     and their scales), 256-byte aligned, owned by the caller.
+ *   - d = 128 only (other d: FA_ERR_UNSUPPORTED).
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d);
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
+                     float* lse, void* workspace, size_t workspace_bytes,
+                     int B, int H, int N, int d, int causal, float scale,
+                     void* stream);
+
+/*
+ * The quantisation step of fa_fwd_fp8 on its own: x bf16 [BH, N, d]
+ * (d = 64 or 128) -> codes E4M3 bytes [BH, N, d] and scales float32
+ * [BH, 8 * ceil(N / 128)] (one per 16-row block; blocks that start at or
+ * past N get scale 1).  x and codes 16-byte aligned; asynchronous on stream.
+ */
+fa_status fa_quantize_e4m3(const void* x, void* codes, float* scales, int BH,
+                           int N, int d, void* stream);
+
+/*
+ * One training step of attention on tensors in HOST memory: copies q, k, v,
+ * dout to the device, runs the forward and the backward, and copies o, lse,
+ * dq, dk, dv back -- the same results as fa_fwd + fa_bwd on device copies.
+ *   - q, k, v, dout, o, dq, dk, dv: host bf16 [B,H,N,d]; lse: host fp32
+ *     [B,H,N].  Page-locked (pinned) host memory lets the copies run
+ *     asynchronously and overlap; pageable memory works but serialises.
+ *   - The B*H heads are processed in chunks of chunk_heads (0: about a
+ *     sixteenth of them): the inputs of the next chunk are copied in and the
+ *     outputs of the previous one copied out on two streams of the library
+ *     while the current chunk computes on `stream`, so the copies in both
+ *     directions overlap each other and the kernels.
+ *   - scratch: device memory of fa_step_host_scratch_size(B, H, N, d,
+ *     chunk_heads) bytes, 256-byte aligned, owned by the caller (three
+ *     rotating chunk slots of tensors and workspace).
+ *   - Asynchronous: the step is ordered after earlier work on `stream`, and
+ *     work submitted to `stream` afterwards (including a synchronisation of
+ *     it) sees every output in host memory.  Calls on one device must not
+ *     overlap each other (they share the library's copy streams).
+ */
+size_t fa_step_host_scratch_size(int B, int H, int N, int d, int chunk_heads);
+fa_status fa_step_host(const void* q, const void* k, const void* v,
+                       const void* dout, void* o, float* lse, void* dq,
+                       void* dk, void* dv, void* scratch, size_t scratch_bytes,
+                       int B, int H, int N, int d, int causal, float scale,
+                       int chunk_heads, void* stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device status record
  * of the current GPU: FA_ERR_DEVICE_TIMEOUT if any kernel of this library
  * gave up on a pipeline wait since the last check, FA_ERR_CUDA if the stream

@@ -26,6 +26,7 @@ def test_header_declares_the_expected_entry_points():
     names = fa.header_functions()
     for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
               "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_ext_workspace_size",
+              "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_quantize_e4m3",
               "fa_check_device_status", "fa_status_string",
               "fa_set_wait_timeout_ns", "fa_debug_expire_wait"):
         assert n in names
@@ -187,3 +188,36 @@ def test_python_binding_checks_grouped_shapes():
         fa._check_ext_shapes(q, k)     # sequence lengths differ
     k = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16)
     assert fa._check_ext_shapes(q, k) == (1, 4, 2, 8, 64)
+
+
+def _fwd_fp8(lib, ptr=256, lse=16, ws=256, ws_bytes=1 << 40, B=1, H=1, N=128,
+             d=128, causal=0, scale=0.125):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_fwd_fp8(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), p(ws),
+                          ws_bytes, B, H, N, d, causal, scale, None)
+
+
+def test_fp8_forward_argument_checks(lib):
+    assert _fwd_fp8(lib, d=64) == UNSUPPORTED
+    assert _fwd_fp8(lib, d=96) == UNSUPPORTED
+    assert _fwd_fp8(lib, scale=0.0) == INVALID
+    assert _fwd_fp8(lib, ptr=0) == INVALID
+    assert _fwd_fp8(lib, ptr=24) == INVALID
+    assert _fwd_fp8(lib, ws=0) == WORKSPACE
+    assert _fwd_fp8(lib, ws=16) == WORKSPACE          # not 256-byte aligned
+    need = lib.fa_fwd_fp8_workspace_size(1, 1, 128, 128)
+    assert _fwd_fp8(lib, ws_bytes=need - 1) == WORKSPACE
+    assert _fwd_fp8(lib, ptr=0, lse=0, ws=0, ws_bytes=0, N=0) == OK
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    assert lib.fa_quantize_e4m3(p(16), p(16), p(16), 2, 100, 96, None) == UNSUPPORTED
+    assert lib.fa_quantize_e4m3(p(0), p(16), p(16), 2, 100, 128, None) == INVALID
+    assert lib.fa_quantize_e4m3(p(0), p(0), p(0), 2, 0, 128, None) == OK
+
+
+@pytest.mark.parametrize("B,H,N,d", [(4, 64, 4096, 128), (1, 3, 333, 128),
+                                     (2, 2, 1, 128)])
+def test_fp8_workspace_size(lib, B, H, N, d):
+    nsb = 8 * ((N + 127) // 128)
+    expect = 2 * _align(B * H * N * d) + 2 * _align(B * H * nsb * 4)
+    assert lib.fa_fwd_fp8_workspace_size(B, H, N, d) == expect
+    assert lib.fa_fwd_fp8_workspace_size(B, H, N, 64) == 0

@@ -115,6 +115,24 @@ fa_status make_acc_map(CUtensorMap* m, const void* base, int BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D view [BH][N][d] of an E4M3 tensor (one byte per element); box = 128
+// rows x 128 bytes (d = 128), 128-byte swizzle.  Rows past N read as zeros.
+fa_status make_fp8_map(CUtensorMap* m, const void* base, int BH, int N,
+                       int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  fa_status s = encode_fn(&fn);
+  if (s != FA_OK) return s;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)N * d};
+  cuuint32_t box[3] = {128, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -191,6 +209,26 @@ WsLayout ws_layout(int B, int H, int Hkv, int N, int d) {
   const size_t kv_acc = w.nsplit > 1 ? align_up(BHkv * N * d * sizeof(float), 256) : 0;
   w.dv_acc_off = w.dk_acc_off + kv_acc;
   w.total = w.dv_acc_off + kv_acc;
+  return w;
+}
+
+// Scale blocks (16 rows) per head, counted over N rounded up to 128.
+int scale_blocks(int N) { return (int)(align_up((size_t)N, fa::kTile) / 16); }
+
+struct Fp8Layout {
+  size_t q8_off, k8_off, sq_off, sk_off, total;
+};
+
+// E4M3 Q | E4M3 K (B*H*N*d bytes each) | Q scales | K scales
+// ([B*H][scale_blocks(N)] float32), each 256-byte aligned.
+Fp8Layout fp8_layout(int B, int H, int N, int d) {
+  const size_t BH = (size_t)B * H;
+  Fp8Layout w;
+  w.q8_off = 0;
+  w.k8_off = align_up(BH * N * d, 256);
+  w.sq_off = w.k8_off + align_up(BH * N * d, 256);
+  w.sk_off = w.sq_off + align_up(BH * scale_blocks(N) * sizeof(float), 256);
+  w.total = w.sk_off + align_up(BH * scale_blocks(N) * sizeof(float), 256);
   return w;
 }
 
@@ -350,6 +388,85 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                     workspace_bytes, B, H, H, N, d, causal, -1, scale, stream);
 }
 
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty || d != 128)
+    return 0;
+  return fp8_layout(B, H, N, d).total;
+}
+
+fa_status fa_quantize_e4m3(const void* x, void* codes, float* scales, int BH,
+                           int N, int d, void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(1, BH, N, d, 0, 1.0f, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!x || !codes || !scales) return FA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4))
+    return FA_ERR_INVALID_ARG;
+  DeviceCtx* ctx = nullptr;
+  if ((s = device_ctx(&ctx)) != FA_OK) return s;
+  cudaError_t e = fa::launch_quant_e4m3(
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(codes),
+      scales, BH, N, d, scale_blocks(N), ctx->sm_count * 8,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
+                     float* lse, void* workspace, size_t workspace_bytes,
+                     int B, int H, int N, int d, int causal, float scale,
+                     void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  const Fp8Layout w = fp8_layout(B, H, N, d);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  DeviceCtx* ctx = nullptr;
+  if ((s = device_ctx(&ctx)) != FA_OK) return s;
+  const int BH = B * H;
+  char* ws = static_cast<char*>(workspace);
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(ws + w.q8_off);
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(ws + w.k8_off);
+  float* sq = reinterpret_cast<float*>(ws + w.sq_off);
+  float* sk = reinterpret_cast<float*>(ws + w.sk_off);
+  CUtensorMap tq, tk, tv;
+  if ((s = make_fp8_map(&tq, q8, BH, N, d)) != FA_OK) return s;
+  if ((s = make_fp8_map(&tk, k8, BH, N, d)) != FA_OK) return s;
+  if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int nsb = scale_blocks(N);
+  cudaError_t e = fa::launch_quant_e4m3(static_cast<const __nv_bfloat16*>(q),
+                                        q8, sq, BH, N, d, nsb,
+                                        ctx->sm_count * 8, st);
+  if (e == cudaSuccess)
+    e = fa::launch_quant_e4m3(static_cast<const __nv_bfloat16*>(k), k8, sk, BH,
+                              N, d, nsb, ctx->sm_count * 8, st);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  fa::FwdArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.H = H;
+  a.Hkv = H;
+  a.window = -1;
+  a.group = BH;
+  a.scale_log2 = scale * fa::kLog2e;
+  a.q_scale = sq;
+  a.k_scale = sk;
+  a.n_sblk = nsb;
+  a.st = ctx->state;
+  a.timeout_ns = g_timeout_ns.load();
+  e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, causal != 0, ctx->sm_count, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 void fa_bwd_set_phase_events(void* before_main, void* after_main) {
   g_ev_before_main = static_cast<cudaEvent_t>(before_main);
   g_ev_after_main = static_cast<cudaEvent_t>(after_main);
@@ -436,6 +553,184 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   }
   return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch,
                 kNoAllocScratchBytes, B, H, N, d, causal, scale, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Training step on host-resident tensors, pipelined by chunks of heads.
+//
+// Heads are independent, so the step runs chunk by chunk (flat head index
+// over B*H; each chunk is one contiguous block of every [B,H,N,d] tensor):
+// the inputs of chunk c+1 are copied in on one stream while chunk c computes
+// on the caller's stream and the outputs of chunk c-1 are copied out on a
+// third, so both copy directions overlap each other and the kernels.  Three
+// device slots (inputs, outputs, backward workspace of one chunk each) rotate
+// over the chunks; a slot is refilled only after the outputs it held have
+// been copied out.
+namespace fa {
+namespace {
+
+constexpr int kSlots = 3;
+// Copy streams per direction (two were measured no faster: the host link,
+// not the number of copy engines, limits the copies).
+constexpr int kCopyStreams = 1;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d[kCopyStreams] = {}, d2h[kCopyStreams] = {};
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[kSlots][kCopyStreams] = {}, comp_done[kSlots] = {},
+              out_done[kSlots][kCopyStreams] = {}, end[kCopyStreams] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+fa_status host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe& p = g_pipe[dev];
+  if (!p.ready) {
+    const unsigned fl = cudaEventDisableTiming;
+    if (cudaEventCreateWithFlags(&p.start, fl) != cudaSuccess) return FA_ERR_CUDA;
+    for (int c = 0; c < kCopyStreams; ++c)
+      if (cudaStreamCreateWithFlags(&p.h2d[c], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&p.d2h[c], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.end[c], fl) != cudaSuccess)
+        return FA_ERR_CUDA;
+    for (int i = 0; i < kSlots; ++i) {
+      if (cudaEventCreateWithFlags(&p.comp_done[i], fl) != cudaSuccess)
+        return FA_ERR_CUDA;
+      for (int c = 0; c < kCopyStreams; ++c)
+        if (cudaEventCreateWithFlags(&p.in_done[i][c], fl) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.out_done[i][c], fl) != cudaSuccess)
+          return FA_ERR_CUDA;
+    }
+    p.ready = true;
+  }
+  *out = &p;
+  return FA_OK;
+}
+
+struct SlotLayout {
+  size_t tensor, lse, ws, total;  // bytes: one [ch,N,d] bf16 tensor, ...
+};
+
+// One slot: q, k, v, dO, O, dQ, dK, dV ([ch,N,d] bf16 each), LSE, and the
+// backward workspace of ch heads, each 256-byte aligned.
+SlotLayout slot_layout(int ch, int N, int d) {
+  SlotLayout s;
+  s.tensor = align_up((size_t)ch * N * d * 2, 256);
+  s.lse = align_up((size_t)ch * N * 4, 256);
+  s.ws = align_up(ws_layout(1, ch, ch, N, d).total, 256);
+  s.total = 8 * s.tensor + s.lse + s.ws;
+  return s;
+}
+
+int chunk_heads_or_default(int BH, int chunk_heads) {
+  if (chunk_heads > 0) return chunk_heads < BH ? chunk_heads : BH;
+  const int c = (BH + 15) / 16;  // about sixteen chunks (measured best)
+  return c > 0 ? c : 1;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_step_host_scratch_size(int B, int H, int N, int d,
+                                            int chunk_heads) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
+  const int ch = fa::chunk_heads_or_default(B * H, chunk_heads);
+  return (size_t)fa::kSlots * fa::slot_layout(ch, N, d).total;
+}
+
+extern "C" fa_status fa_step_host(const void* q, const void* k, const void* v,
+                                  const void* dout, void* o, float* lse,
+                                  void* dq, void* dk, void* dv, void* scratch,
+                                  size_t scratch_bytes, int B, int H, int N,
+                                  int d, int causal, float scale,
+                                  int chunk_heads, void* stream) {
+  bool empty = false;
+  fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (chunk_heads < 0) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !dout || !o || !lse || !dq || !dk || !dv)
+    return FA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  const int ch = fa::chunk_heads_or_default(BH, chunk_heads);
+  const fa::SlotLayout L = fa::slot_layout(ch, N, d);
+  if (!scratch || !aligned(scratch, 256) ||
+      scratch_bytes < (size_t)fa::kSlots * L.total)
+    return FA_ERR_WORKSPACE;
+  fa::HostPipe* p = nullptr;
+  if ((s = fa::host_pipe(&p)) != FA_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // Everything already on the caller's stream comes first.
+  if (cudaEventRecord(p->start, cs) != cudaSuccess) return FA_ERR_CUDA;
+  for (int c = 0; c < fa::kCopyStreams; ++c)
+    if (cudaStreamWaitEvent(p->h2d[c], p->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(p->d2h[c], p->start, 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+  const size_t row_bytes = (size_t)N * d * 2;  // one head of one tensor
+  const int n_chunks = (BH + ch - 1) / ch;
+  const void* in_h[4] = {q, k, v, dout};
+  void* out_h[4] = {o, dq, dk, dv};
+  for (int c = 0; c < n_chunks; ++c) {
+    const int slot = c % fa::kSlots;
+    const int h0 = c * ch;
+    const int hc = BH - h0 < ch ? BH - h0 : ch;
+    char* base = static_cast<char*>(scratch) + (size_t)slot * L.total;
+    char* t[8];
+    for (int i = 0; i < 8; ++i) t[i] = base + (size_t)i * L.tensor;
+    float* lse_d = reinterpret_cast<float*>(base + 8 * L.tensor);
+    void* ws_d = base + 8 * L.tensor + L.lse;
+    const size_t bytes = (size_t)hc * row_bytes;
+    // inputs of chunk c, tensor i on copy stream i % kCopyStreams, after the
+    // slot's previous outputs have left
+    for (int cc = 0; cc < fa::kCopyStreams; ++cc)
+      if (c >= fa::kSlots)
+        for (int dc = 0; dc < fa::kCopyStreams; ++dc)
+          if (cudaStreamWaitEvent(p->h2d[cc], p->out_done[slot][dc], 0) != cudaSuccess)
+            return FA_ERR_CUDA;
+    for (int i = 0; i < 4; ++i)
+      if (cudaMemcpyAsync(t[i], static_cast<const char*>(in_h[i]) + (size_t)h0 * row_bytes,
+                          bytes, cudaMemcpyHostToDevice,
+                          p->h2d[i % fa::kCopyStreams]) != cudaSuccess)
+        return FA_ERR_CUDA;
+    for (int cc = 0; cc < fa::kCopyStreams; ++cc)
+      if (cudaEventRecord(p->in_done[slot][cc], p->h2d[cc]) != cudaSuccess ||
+          cudaStreamWaitEvent(cs, p->in_done[slot][cc], 0) != cudaSuccess)
+        return FA_ERR_CUDA;
+    // compute on the caller's stream
+    if ((s = fa_fwd(t[0], t[1], t[2], t[4], lse_d, 1, hc, N, d, causal, scale,
+                    stream)) != FA_OK)
+      return s;
+    if ((s = fa_bwd(t[0], t[1], t[2], t[4], lse_d, t[3], t[5], t[6], t[7],
+                    ws_d, L.ws, 1, hc, N, d, causal, scale, stream)) != FA_OK)
+      return s;
+    if (cudaEventRecord(p->comp_done[slot], cs) != cudaSuccess) return FA_ERR_CUDA;
+    for (int cc = 0; cc < fa::kCopyStreams; ++cc)
+      if (cudaStreamWaitEvent(p->d2h[cc], p->comp_done[slot], 0) != cudaSuccess)
+        return FA_ERR_CUDA;
+    // outputs of chunk c
+    for (int i = 0; i < 4; ++i)
+      if (cudaMemcpyAsync(static_cast<char*>(out_h[i]) + (size_t)h0 * row_bytes,
+                          t[4 + i], bytes, cudaMemcpyDeviceToHost,
+                          p->d2h[i % fa::kCopyStreams]) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaMemcpyAsync(lse + (size_t)h0 * N, lse_d, (size_t)hc * N * 4,
+                        cudaMemcpyDeviceToHost, p->d2h[0]) != cudaSuccess)
+      return FA_ERR_CUDA;
+    for (int cc = 0; cc < fa::kCopyStreams; ++cc)
+      if (cudaEventRecord(p->out_done[slot][cc], p->d2h[cc]) != cudaSuccess)
+        return FA_ERR_CUDA;
+  }
+  // Later work on the caller's stream sees every output on the host.
+  for (int c = 0; c < fa::kCopyStreams; ++c)
+    if (cudaEventRecord(p->end[c], p->d2h[c]) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, p->end[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 namespace fa {

@@ -116,6 +116,18 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc,
   }
 }
 
+// FP8 path: S_t = Q8_t K8^T with E4M3 operands, K = d = 128 in four steps
+// of 32 elements (32 bytes) along one 128-byte row; scales are applied by
+// the softmax.
+__device__ __forceinline__ void issue_qk_fp8(uint32_t s_tmem, uint64_t q_desc,
+                                             uint64_t k_desc) {
+  constexpr uint32_t id = idesc_e4m3(128, 128);
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+    mma_ss_f8(s_tmem, sdesc_adv(q_desc, s * 32), sdesc_adv(k_desc, s * 32), id,
+              s > 0 ? 1u : 0u);
+}
+
 // O_t (+)= P_t V: M = 128, N = d, K = 128 keys; A = P from TMEM, B = V
 // read MN-major (d contiguous in smem; 16 keys = 2048 bytes per K step).
 // v_desc: MN-major descriptor of V's first byte.
@@ -195,13 +207,18 @@ __device__ __forceinline__ int fwd_round_item(int r) {
 // phases run on across items, so the producer fetches the next item's Q and
 // K/V while the current one finishes, and the next item's first Q K^T
 // overlaps the softmax warps' epilogue.
-template <int D, bool CAUSAL, bool WINDOW>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = FwdLayout<D>;
   constexpr int S = L::kStages;
+  // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 (one
+  // byte per element, d = 128: a single box) on the FP8 path.
+  static_assert(!FP8 || D == 128, "the FP8 path needs d = 128");
+  constexpr uint32_t kQKBytes = FP8 ? kTile * D : L::kTileBytes;
+  constexpr int kQKBoxes = FP8 ? 1 : L::kSub;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   auto* bars = reinterpret_cast<FwdBars<S>*>(smem + L::kBarOff);
@@ -264,9 +281,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // Q_t must no longer be read by the previous item's Q K^T.
           ok = wait_bar<kInl>(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->q_full[t], L::kTileBytes);
+          mbar_arrive_expect_tx(&bars->q_full[t], kQKBytes);
 #pragma unroll
-          for (int sb = 0; sb < L::kSub; ++sb)
+          for (int sb = 0; sb < kQKBoxes; ++sb)
             tma_load_3d(smem + L::kQOff + t * L::kTileBytes + sb * kSubTileBytes,
                         &tm_q, &bars->q_full[t], sb * 64,
                         (t ? itm.qt1 : itm.qt0) * kTile, itm.bh);
@@ -276,10 +293,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int kv = 0; kv < 2; ++kv) {  // 0: K_j, 1: V_j
             ok = wait_bar<kInl>(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
             if (!ok) break;
-            mbar_arrive_expect_tx(&bars->kv_full[stage], L::kTileBytes);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
-#pragma unroll
-            for (int sb = 0; sb < L::kSub; ++sb)
+            const int boxes = kv ? L::kSub : kQKBoxes;
+            mbar_arrive_expect_tx(&bars->kv_full[stage],
+                                  kv ? (uint32_t)L::kTileBytes : kQKBytes);
+            for (int sb = 0; sb < boxes; ++sb)
               tma_load_3d(smem + L::kKVOff + stage * L::kTileBytes +
                               sb * kSubTileBytes,
                           m, &bars->kv_full[stage], sb * 64, j * kTile, itm.kvh);
@@ -333,7 +351,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // Q K^T for tile t and key tile x; after the tile's last one (hi_t),
       // Q_t is released to the producer (in-order completion).
       auto qk = [&](int t, int x, int hi_t, int k_st) {
-        issue_qk<D>(tS(t), q_desc(t), k_desc(k_st));
+        if constexpr (FP8)
+          issue_qk_fp8(tS(t), q_desc(t), k_desc(k_st));
+        else
+          issue_qk<D>(tS(t), q_desc(t), k_desc(k_st));
         mma_commit(&bars->s_full[t]);
         if (x == hi_t) mma_commit(&bars->q_empty[t]);
       };
@@ -427,8 +448,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int klo_max = WINDOW ? q0 + kTile - 1 - win : -1;
       const int khi_min =
           CAUSAL ? q0 : (WINDOW ? (q0 > nm1 - win ? nm1 : q0 + win) : nm1);
+      // FP8: scores are in units of sq(row block) * sk(key block); the row's
+      // factor is folded into its exponent scale.
+      float cr = c;
+      if constexpr (FP8) cr = c * a.q_scale[(size_t)itm.bh * a.n_sblk + (qrow >> 4)];
       float m_ref = -INFINITY, l = 0.f;
       for (int j = lo_t; j <= hi_t; ++j) {
+        float4 ska, skb;  // FP8: the 8 key-block scales of tile j
+        if constexpr (FP8) {
+          const float4* ks = reinterpret_cast<const float4*>(
+              a.k_scale + (size_t)itm.kvh * a.n_sblk + (size_t)j * 8);
+          ska = ks[0];
+          skb = ks[1];
+        }
         ok = wait_bar_warp<kInl>(&bars->s_full[t], s_cnt & 1u, wc, kWFwdSmS);
         ++s_cnt;
         if (!ok) break;
@@ -463,19 +495,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         // Row max: four independent chains of three-input maxima (one long
-        // dependent chain dominated the softmax latency).
-        float mx4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mx4[k] = fmaxf(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
-#pragma unroll
-        for (int e = 8; e < 128; e += 8)
+        // dependent chain dominated the softmax latency).  FP8: one maximum
+        // per 16-key group, each times its positive scale.
+        float m_tile;
+        float w[8];  // FP8: exponent scale of each 16-key group
+        if constexpr (!FP8) {
+          float mx4[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mx4[k] = max3(mx4[k], __uint_as_float(s[e + 2 * k]),
-                          __uint_as_float(s[e + 2 * k + 1]));
-        const float mx = max3(max3(mx4[0], mx4[1], mx4[2]), mx4[3], mx4[3]);
-        const float m_tile = mx * c;
+            mx4[k] = fmaxf(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
+#pragma unroll
+          for (int e = 8; e < 128; e += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mx4[k] = max3(mx4[k], __uint_as_float(s[e + 2 * k]),
+                            __uint_as_float(s[e + 2 * k + 1]));
+          const float mx = max3(max3(mx4[0], mx4[1], mx4[2]), mx4[3], mx4[3]);
+          m_tile = mx * c;
+        } else {
+          w[0] = cr * ska.x; w[1] = cr * ska.y; w[2] = cr * ska.z; w[3] = cr * ska.w;
+          w[4] = cr * skb.x; w[5] = cr * skb.y; w[6] = cr * skb.z; w[7] = cr * skb.w;
+          float mg[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float m = fmaxf(__uint_as_float(s[16 * g]), __uint_as_float(s[16 * g + 1]));
+#pragma unroll
+            for (int e = 16 * g + 2; e < 16 * g + 16; e += 2)
+              m = max3(m, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+            mg[g] = m * w[g];
+          }
+          m_tile = max3(max3(mg[0], mg[1], mg[2]), max3(mg[3], mg[4], mg[5]),
+                        fmaxf(mg[6], mg[7]));
+        }
         // Lazy rescale: keep the reference max until the row max exceeds it
         // by more than the threshold; exp2(x - m_ref) <= 2^8 meanwhile.
         const bool bump = m_tile > m_ref + kRescaleThreshold;
@@ -490,6 +541,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float neg_m = -m_ref;
         if constexpr (WINDOW) neg_m = (m_ref == -INFINITY) ? 0.f : neg_m;
         const uint64_t c2 = bcast2(c), nm2 = bcast2(neg_m);
+        uint64_t w2[8];
+        if constexpr (FP8) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) w2[g] = bcast2(w[g]);
+        }
         // Scores to exponents two at a time (packed fp32 FMA), row sum in
         // four packed partial sums; P is packed in place: pair (e, e+1) goes
         // to s[e/2], a slot whose score has already been consumed.
@@ -498,7 +554,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int e = 0; e < 128; e += 2) {
           float x0, x1;
           fma2_bcast(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]),
-                     c2, nm2);
+                     FP8 ? w2[e / 16] : c2, nm2);
           const float p0 = ex2(x0), p1 = ex2(x1);
           add2_acc(la[(e >> 1) & 3], lb[(e >> 1) & 3], p0, p1);
           s[e / 2] = pack_bf16(p0, p1);
@@ -569,12 +625,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool WINDOW>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, WINDOW>;
+  auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8>;
   cudaError_t e;
   if constexpr (kSplitRegs) {
     // The register split inside the kernel assumes exactly kLaunchRegs per
@@ -600,11 +656,92 @@ cudaError_t launch_fwd_w(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
   return a.window >= 0
-             ? launch_fwd_t<D, CAUSAL, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-             : launch_fwd_t<D, CAUSAL, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+             ? launch_fwd_t<D, CAUSAL, true, false>(tq, tk, tv, a, BH, grid_blocks, stream)
+             : launch_fwd_t<D, CAUSAL, false, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+}
+
+// E4M3 quantisation, one warp per 16-row block of one head: amax of the
+// block, scale = amax / 448 (1 for an all-zero block), codes = round to
+// nearest even of x / scale with saturation.  Both divisions are IEEE
+// round-to-nearest, so the codes are those of the same float32 arithmetic
+// anywhere.  Lane l holds columns [l*D/32, (l+1)*D/32) of every row.
+template <int D>
+__global__ void __launch_bounds__(256) quant_e4m3_kernel(
+    const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
+    float* __restrict__ scales, int BH, int N, int n_sblk) {
+  constexpr int kPer = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long n_blk = (long long)BH * n_sblk;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long blk = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       blk < n_blk; blk += warps) {
+    const int bh = (int)(blk / n_sblk);
+    const int r0 = (int)(blk - (long long)bh * n_sblk) * 16;
+    const int rows = N - r0 < 16 ? N - r0 : 16;
+    if (rows <= 0) {  // padding block past N
+      if (lane == 0) scales[blk] = 1.0f;
+      continue;
+    }
+    const size_t base = ((size_t)bh * N + r0) * D + lane * kPer;
+    float v[16][kPer];
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < rows) {
+        if constexpr (kPer == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(x + base + (size_t)r * D);
+          v[r][0] = bf16_lo(u.x); v[r][1] = bf16_hi(u.x);
+          v[r][2] = bf16_lo(u.y); v[r][3] = bf16_hi(u.y);
+        } else {
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(x + base + (size_t)r * D);
+          v[r][0] = bf16_lo(u); v[r][1] = bf16_hi(u);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) v[r][e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r >= rows) break;
+      uint8_t* dst = codes + base + (size_t)r * D;
+      if constexpr (kPer == 4) {
+        const uint32_t lo = pack_e4m3(__fdiv_rn(v[r][0], sc), __fdiv_rn(v[r][1], sc));
+        const uint32_t hi = pack_e4m3(__fdiv_rn(v[r][2], sc), __fdiv_rn(v[r][3], sc));
+        *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
+      } else {
+        *reinterpret_cast<uint16_t*>(dst) =
+            pack_e4m3(__fdiv_rn(v[r][0], sc), __fdiv_rn(v[r][1], sc));
+      }
+    }
+    if (lane == 0) scales[blk] = sc;
+  }
 }
 
 }  // namespace
+
+cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
+                              float* scales, int BH, int N, int d, int n_sblk,
+                              int grid_blocks, cudaStream_t stream) {
+  if (d == 128)
+    quant_e4m3_kernel<128><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N, n_sblk);
+  else
+    quant_e4m3_kernel<64><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N, n_sblk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdArgs& a, int BH,
+                           bool causal, int grid_blocks, cudaStream_t stream) {
+  return causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                : launch_fwd_t<128, false, false, true>(tq, tk, tv, a, BH, grid_blocks, stream);
+}
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,

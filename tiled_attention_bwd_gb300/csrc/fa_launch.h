@@ -20,6 +20,11 @@ struct FwdArgs {
   int window;           // band half-width in keys, < 0: none
   int group;            // heads per scheduling group
   float scale_log2;     // scale * log2(e): scores enter exp2 directly
+  // FP8 path only: per-16-row-block scales of the E4M3 Q and K,
+  // [BH or BHkv][n_sblk] with n_sblk = N rounded up to 128, over 16.
+  const float* q_scale;
+  const float* k_scale;
+  int n_sblk;
   DevState* st;
   uint64_t timeout_ns;
 };
@@ -56,6 +61,16 @@ struct BwdArgs {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
                        bool causal, int grid_blocks, cudaStream_t stream);
+// FP8 forward: tq, tk are E4M3 tensor maps (one byte per element), tv the
+// bf16 V map; d = 128 only.
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdArgs& a, int BH,
+                           bool causal, int grid_blocks, cudaStream_t stream);
+// E4M3 codes and per-16-row-block scales of a bf16 [BH, N, d] tensor
+// (d = 64 or 128); scales has BH * n_sblk entries, 1 for blocks past N.
+cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
+                              float* scales, int BH, int N, int d, int n_sblk,
+                              int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
                            cudaStream_t stream);
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,

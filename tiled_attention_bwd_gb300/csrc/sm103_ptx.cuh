@@ -154,6 +154,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn,
          | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B
+// (format code 0), fp32 accumulator, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                          // D format: f32
+         | (0u << 7)                        // A format: E4M3
+         | (0u << 10)                       // B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   K-major : rows of 128 bytes along K, 8-row atoms 1024 bytes apart (sbo);
 //             lbo is unused.
@@ -185,6 +195,18 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], 8-bit floating-point operands (K = 32).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
@@ -327,6 +349,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two float32 values to E4M3 bytes (round to nearest even, saturating at
+// +-448): `lo` in the low byte, `hi` in the high byte.
+__device__ __forceinline__ uint16_t pack_e4m3(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) {

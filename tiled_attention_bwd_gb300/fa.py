@@ -66,6 +66,18 @@ def open_library(path: str):
     lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
     lib.fa_bwd_ext.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                               i, i, i, i, i, f, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
+    lib.fa_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, vp]
+    lib.fa_quantize_e4m3.restype = i
+    lib.fa_step_host_scratch_size.argtypes = [i, i, i, i, i]
+    lib.fa_step_host_scratch_size.restype = ctypes.c_size_t
+    lib.fa_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 ctypes.c_size_t, i, i, i, i, i, f, i, vp]
+    lib.fa_step_host.restype = i
     lib.fa_bwd_ext_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_ext_workspace_size.restype = ctypes.c_size_t
     lib.fa_check_device_status.argtypes = [vp]
@@ -281,6 +293,98 @@ def fa_bwd_ext(q, k, v, o, lse, dout, causal: bool, scale: float,
             int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))
     return dq, dk, dv
+
+
+def fa_fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_size(B, H, N, d))
+
+
+def fa_fwd_fp8(q, k, v, causal: bool, scale: float, out=None, lse=None,
+               workspace=None):
+    """FP8 forward: Q and K quantised to E4M3 per 16-row block, Q K^T on
+    the FP8 tensor cores.  Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
+    lib = load_library()
+    _check_qkv("q", q)
+    _check_qkv("k", k, q.shape)
+    _check_qkv("v", v, q.shape)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_qkv("out", out, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    if workspace is None:
+        need = fa_fwd_fp8_workspace_size(B, H, N, d)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8,
+                                device=q.device)
+    with torch.cuda.device(q.device):
+        _check("fa_fwd_fp8", lib.fa_fwd_fp8(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), B, H, N, d,
+            int(bool(causal)), float(scale), _stream_handle(q.device)))
+    return out, lse
+
+
+def fa_quantize_e4m3(x):
+    """E4M3 codes (uint8, same shape) and per-16-row-block scales (fp32
+    [..., 8 * ceil(N / 128)]) of a bf16 [..., N, d] CUDA tensor."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 \
+            or not x.is_cuda or x.dim() < 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [..., N, d]")
+    *lead, N, d = x.shape
+    BH = 1
+    for n in lead:
+        BH *= n
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((*lead, 8 * ((N + 127) // 128)), dtype=torch.float32,
+                         device=x.device)
+    with torch.cuda.device(x.device):
+        _check("fa_quantize_e4m3", lib.fa_quantize_e4m3(
+            _ptr(x), _ptr(codes), _ptr(scales), BH, N, d,
+            _stream_handle(x.device)))
+    return codes, scales
+
+
+def fa_step_host_scratch_size(B: int, H: int, N: int, d: int,
+                              chunk_heads: int = 0) -> int:
+    return int(load_library().fa_step_host_scratch_size(B, H, N, d,
+                                                        chunk_heads))
+
+
+def fa_step_host(q, k, v, dout, causal: bool, scale: float, o, lse, dq, dk,
+                 dv, scratch=None, chunk_heads: int = 0, device=None):
+    """Forward + backward on HOST tensors (bf16 [B,H,N,d]; lse fp32
+    [B,H,N]; pinned memory for overlap), pipelined by chunks of heads on
+    `device`.  Outputs are written into o, lse, dq, dk, dv; the call is
+    asynchronous on the device's current stream."""
+    lib = load_library()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout), ("o", o),
+                    ("dq", dq), ("dk", dk), ("dv", dv)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or \
+                t.dtype != torch.bfloat16 or t.dim() != 4 or \
+                not t.is_contiguous() or tuple(t.shape) != tuple(q.shape):
+            raise ValueError("%s must be a contiguous bf16 host tensor of "
+                             "q's shape" % name)
+    B, H, N, d = q.shape
+    if lse.is_cuda or lse.dtype != torch.float32 or \
+            tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 host tensor [B,H,N]")
+    if scratch is None:
+        need = fa_step_host_scratch_size(B, H, N, d, chunk_heads)
+        scratch = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("fa_step_host", lib.fa_step_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(scratch),
+            scratch.numel() * scratch.element_size(), B, H, N, d,
+            int(bool(causal)), float(scale), int(chunk_heads),
+            _stream_handle(dev)))
+    return o, lse, dq, dk, dv
 
 
 def fa_bwd_noalloc_max_workspace() -> int:
