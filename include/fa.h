@@ -80,7 +80,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
 /*
  * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,N,d] followed by two fp32 per-row vectors
- * (D_i = dO_i . O_i and LSE_i * log2(e)) padded to whole 128-row tiles.
+ * (D_i = dO_i . O_i and -LSE_i * log2(e)) padded to whole 128-row tiles.
  * Returns 0 for an empty problem or unsupported d.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

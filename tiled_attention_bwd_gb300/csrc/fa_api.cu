@@ -96,8 +96,9 @@ fa_status make_tile_map(CUtensorMap* m, const void* base, int BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D view [BH][N][d] of the fp32 dQ accumulator; box = 128 rows x 32
-// columns (128 bytes), 128-byte swizzle.  Reduce-adds clip rows past N.
+// 3-D view [BH][N][d] of the fp32 dQ accumulator; box = 32 rows x 32
+// columns (128 bytes), 128-byte swizzle: one drain warp's rows of one
+// 32-column group.  Reduce-adds clip rows past N.
 fa_status make_acc_map(CUtensorMap* m, const void* base, int BH, int N,
                        int d) {
   PFN_cuTensorMapEncodeTiled_v12000 fn;
@@ -105,7 +106,7 @@ fa_status make_acc_map(CUtensorMap* m, const void* base, int BH, int N,
   if (s != FA_OK) return s;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  cuuint32_t box[3] = {32, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                   const_cast<void*>(base), dims, strides, box, estr,

@@ -9,25 +9,29 @@
 //   dK = scale dS^T Q.
 //
 // Three launches on one stream:
-//   pre   D_i and LSE_i*log2(e) per row (padded to whole tiles: D = 0 and
-//         LSE2 = +inf past N, which zeroes P there); dQ accumulator := 0.
+//   pre   D_i and LSE2_i = -LSE_i*log2(e) per row (padded to whole tiles:
+//         D = 0 and LSE2 = -inf past N, which zeroes P there); dQ
+//         accumulator := 0.
 //   main  one thread block per (batch, head, 128-key tile j).  K_j, V_j stay
 //         in smem; dK_j, dV_j accumulate in TMEM; Q_i (two stages) and dO_i
 //         (one buffer) stream in by TMA (causal: only i >= j).  Per Q tile, five tcgen05
 //         MMAs: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P^T from TMEM),
-//         dK += dS^T Q and dQ_i = dS K (dS from smem, read K-major for the
-//         first and MN-major for the second).  dQ_i leaves TMEM and is
-//         added into the fp32 accumulator by TMA reduce-add.
+//         dK += dS^T Q (dS^T from TMEM) and dQ_i = dS K (dS from smem, read
+//         MN-major).  dQ_i leaves TMEM and is added into the fp32
+//         accumulator by TMA reduce-add.
 //   post  dQ = scale * accumulator, rounded to bf16.
 //
 // Warps of the main kernel:
-//   0-3  thread = key row: P^T = exp2(S^T c - LSE2), then dS^T = P^T (dP^T - D)
+//   0-3  thread = key row: P^T = exp2(S^T c + LSE2), then dS^T = P^T (dP^T - D)
 //   4-7  thread = query row: drain dQ_i from TMEM, stage it box by box
 //        through two 16 KB buffers and add it into the fp32 accumulator with
 //        TMA reduce-add
 //   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
-// TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T and then dQ [128,256)
-// dK [256, 256+d)  dV [256+d, 256+2d).
+// TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T, then dS^T (bf16
+// pairs in [128,192)), then dQ [128,256)  dK [256, 256+d)  dV [256+d, 256+2d).
+// Measured on this part, an M=128 N=128 MMA with both operands in smem runs
+// at about 40% of the tensor rate and one with A in TMEM at full rate, so
+// every product whose A operand can live in TMEM takes it from there.
 #include <climits>
 
 #include "fa_common.cuh"
@@ -54,10 +58,11 @@ struct BwdLayout {
   static constexpr int kDOOff = kQOff + 2 * kQStageBytes;
   static constexpr int kDSOff = kDOOff + kTileBytes;
   static constexpr int kDSBytes = kTile * kTile * 2;  // 2 sub-tiles [128][64]
-  // dQ staging: two [128 rows][32 fp32] boxes of 16 KB, used alternately.
+  // dQ staging: per drain warp two [32 rows][32 fp32] boxes of 4 KB, used
+  // alternately (4 warps x 2 x 4 KB).
   static constexpr int kStgOff = kDSOff + kDSBytes;
-  static constexpr int kStgBoxBytes = kTile * 128;
-  static constexpr int kBarOff = kStgOff + 2 * kStgBoxBytes;
+  static constexpr int kStgBoxBytes = 32 * 128;
+  static constexpr int kBarOff = kStgOff + 8 * kStgBoxBytes;
   // d = 128 uses 231,680 of the 232,448 bytes a block may have, so the base
   // is taken as is (checked at run time); d = 64 keeps alignment slack.
   static constexpr int kSlack = (D == 128) ? 0 : 1024;
@@ -77,8 +82,6 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t ds_free;
-  uint64_t stg_ready[2];
-  uint64_t stg_free[2];
   uint64_t acc_done;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -101,8 +104,6 @@ enum : uint32_t {
   kWBwdCmpAcc = 0x315,
   kWBwdDqFull = 0x411,
   kWBwdDqAcc = 0x412,
-  kWBwdDqStgFree = 0x413,
-  kWBwdDqStgReady = 0x414,
   kWBwdMisaligned = 0x5A1,
 };
 
@@ -217,8 +218,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
-      mbar_init(&bars->stg_ready[s], 4);  // one arrival per drain warp
-      mbar_init(&bars->stg_free[s], 1);
     }
     mbar_init(&bars->do_full, 1);
     mbar_init(&bars->do_empty, 1);
@@ -320,7 +319,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t v_km = sdesc_sw128(smem_addr(v_s), 16, 1024);
       const uint64_t do_km = sdesc_sw128(smem_addr(do_s), 16, 1024);
       const uint64_t do_mn = sdesc_sw128(smem_addr(do_s), kSubTileBytes, 1024);
-      const uint64_t ds_km = sdesc_sw128(smem_addr(ds_s), 16, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_addr(ds_s), kSubTileBytes, 1024);
       const uint64_t q_km0 = sdesc_sw128(smem_addr(smem + L::kQOff), 16, 1024);
       const uint64_t q_mn0 =
@@ -383,11 +381,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
         if (!ok) break;
         tc_fence_after();
-        // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T K-major in smem
+        // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T from TMEM (bf16
+        // pairs in the dP^T columns), Q read MN-major
         const uint64_t qmn = q_mn(it);
 #pragma unroll
         for (int s = 0; s < kTile / 16; ++s)
-          mma_ss(tDK, sdesc_adv(ds_km, kstep(s)), sdesc_adv(qmn, s * 2048), id_kv,
+          mma_ts(tDK, tDP + s * 8, sdesc_adv(qmn, s * 2048), id_kv,
                  (it > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bars->q_empty[it & 1]);   // Q_i, LSE2_i, D_i released
         // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
@@ -416,6 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = quarter * 32 + lane;                  // key row in tile j
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const float c = a.scale_log2;
+    const uint64_t c2 = bcast2(c);
     bool ok = run;
     // Band: query q (global) sees key k when dmin <= q - k <= dmax (INT_MIN /
     // INT_MAX: no bound); a tile pair needs the mask only if its offsets
@@ -432,13 +432,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t par = (uint32_t)(it & 1);
       ok = wait_bar_warp(&bars->q_full[stage], sp, wc, kWBwdCmpQ);
       if (!ok) break;
-      const float* lse2 = reinterpret_cast<const float*>(
+      // -LSE_i log2(e) and D_i of this Q tile's rows, in smem after Q_i
+      const float* nlse2 = reinterpret_cast<const float*>(
           smem + L::kQOff + stage * L::kQStageBytes + L::kTileBytes);
-      const float* dd = lse2 + kTile;
+      const float* dd = nlse2 + kTile;
       ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
       if (!ok) break;
       tc_fence_after();
-      // P^T = exp2(S^T c - LSE2), in two halves of 64 queries so that only
+      // P^T = exp2(S^T c + LSE2) (LSE2 = -LSE log2 e; packed pairs), in two
+      // halves of 64 queries so that only
       // half a row of S is live; P half h goes to TMEM columns [32h, 32h+32),
       // over S columns that have already been read.
       uint32_t pk[64];
@@ -465,11 +467,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; e += 4) {
           const int q = 64 * h + e;
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
-          float x0 = fmaf(__uint_as_float(s[e + 0]), c, -l4.x);
-          float x1 = fmaf(__uint_as_float(s[e + 1]), c, -l4.y);
-          float x2 = fmaf(__uint_as_float(s[e + 2]), c, -l4.z);
-          float x3 = fmaf(__uint_as_float(s[e + 3]), c, -l4.w);
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + q);
+          float x0, x1, x2, x3;
+          fma2_bc(x0, x1, __uint_as_float(s[e + 0]), __uint_as_float(s[e + 1]),
+                  c2, l4.x, l4.y);
+          fma2_bc(x2, x3, __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]),
+                  c2, l4.z, l4.w);
           pk[q / 2] = pack_bf16(ex2(x0), ex2(x1));
           pk[q / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
         }
@@ -493,6 +496,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok && it > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
       if (!ok) break;
       tc_fence_after();
+      // dS^T goes to smem (read MN-major as dS by the dQ MMA) and, packed to
+      // bf16 pairs, into TMEM columns [128, 192) over dP^T values already
+      // read (the dK MMA takes it from there as its A operand): chunk ch
+      // (32 queries) fills columns 128 + 16 ch .. 128 + 16 ch + 15, which
+      // held dP^T of chunk ch / 2, already loaded.
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t dp[32];
@@ -505,10 +513,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int q = ch * 32 + e;
           const float4 d4 = *reinterpret_cast<const float4*>(dd + q);
           const uint32_t pa = pk[q / 2], pb = pk[q / 2 + 1];
-          const float ds0 = bf16_lo(pa) * (__uint_as_float(dp[e + 0]) - d4.x);
-          const float ds1 = bf16_hi(pa) * (__uint_as_float(dp[e + 1]) - d4.y);
-          const float ds2 = bf16_lo(pb) * (__uint_as_float(dp[e + 2]) - d4.z);
-          const float ds3 = bf16_hi(pb) * (__uint_as_float(dp[e + 3]) - d4.w);
+          float ds0, ds1, ds2, ds3;
+          mulsub2(ds0, ds1, bf16_lo(pa), bf16_hi(pa), __uint_as_float(dp[e + 0]),
+                  __uint_as_float(dp[e + 1]), d4.x, d4.y);
+          mulsub2(ds2, ds3, bf16_lo(pb), bf16_hi(pb), __uint_as_float(dp[e + 2]),
+                  __uint_as_float(dp[e + 3]), d4.z, d4.w);
           dsk[e / 2] = pack_bf16(ds0, ds1);
           dsk[e / 2 + 1] = pack_bf16(ds2, ds3);
         }
@@ -521,7 +530,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               make_uint4(dsk[4 * g], dsk[4 * g + 1], dsk[4 * g + 2],
                          dsk[4 * g + 3]);
         }
+        tmem_st16(tl + 128 + ch * 16, dsk);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(&bars->ds_full);
@@ -536,14 +547,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
     // dQ_i leaves TMEM into registers (then the columns are released) and is
-    // added into the fp32 accumulator box by box ([128 rows][32 fp32] = 16 KB
-    // in the 128-byte swizzle layout) through two staging buffers used
-    // alternately, by TMA reduce-add (whole 128-byte lines at L2).  A buffer
-    // is rewritten only after the TMA has read the box before the last one.
+    // added into the fp32 accumulator by TMA reduce-add (whole 128-byte
+    // lines at L2).  Each warp handles its own 32 rows independently: box by
+    // box ([32 rows][32 fp32] = 4 KB in the 128-byte swizzle layout) through
+    // two staging buffers of its own, rewriting a buffer only after the TMA
+    // has read the box before the last one (bulk groups are per thread, and
+    // lane 0 issues and waits on all of this warp's).
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const bool elected = (warp == 4 && lane == 0);
+    uint8_t* const stg_w = stg_s + quarter * 2 * L::kStgBoxBytes;
     constexpr int kBoxes = D / 32;
     int g = 0;                                       // boxes staged so far
     bool ok = run;
@@ -563,43 +576,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       warp_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
 #pragma unroll
       for (int b = 0; b < kBoxes; ++b, ++g) {
-        const int buf = g & 1;
+        uint8_t* const buf = stg_w + (g & 1) * L::kStgBoxBytes;
         if (g >= 2) {
-          ok = wait_bar_warp(&bars->stg_free[buf], (uint32_t)(((g >> 1) - 1) & 1),
-                             wc, kWBwdDqStgFree);
-          if (!ok) break;
+          if (lane == 0) bulk_wait_read_allbut1();  // box g-2 has been read
+          __syncwarp();
         }
-        uint8_t* dst = stg_s + buf * L::kStgBoxBytes + r * 128;
+        uint8_t* dst = buf + lane * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) * 16)) =
+          *reinterpret_cast<uint4*>(dst + ((k ^ (lane & 7)) * 16)) =
               make_uint4(acc[32 * b + 4 * k], acc[32 * b + 4 * k + 1],
                          acc[32 * b + 4 * k + 2], acc[32 * b + 4 * k + 3]);
         fence_proxy_async_smem();
-        warp_arrive(&bars->stg_ready[buf]);
-        if (elected) {
-          ok = wait_bar(&bars->stg_ready[buf], (uint32_t)((g >> 1) & 1), wc,
-                        kWBwdDqStgReady);
-          if (ok) {
-            tma_reduce_add_3d(&tm_dq, stg_s + buf * L::kStgBoxBytes, b * 32,
-                              i * kTile, bh);
-            bulk_commit_group();
-          }
-          if (b > 0) {
-            // The previous box (other buffer) has been read: release it.
-            bulk_wait_read_allbut1();
-            mbar_arrive(&bars->stg_free[buf ^ 1]);
-          }
-          if (b == kBoxes - 1) {
-            bulk_wait_read_all();
-            mbar_arrive(&bars->stg_free[buf]);
-          }
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, buf, b * 32, i * kTile + quarter * 32, bh);
+          bulk_commit_group();
         }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
       }
     }
-    if (elected) bulk_wait_all();  // accumulator adds complete before exit
+    if (lane == 0) bulk_wait_all();  // accumulator adds complete before exit
     // dV epilogue (rows = keys)
     if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdDqAcc);
     if (ok) {
@@ -618,7 +614,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// D_i = dO_i . O_i and LSE2_i = LSE_i log2(e) for every padded row (one warp
+// D_i = dO_i . O_i and LSE2_i = -LSE_i log2(e) for every padded row (one warp
 // per row, four rows in flight per warp); then the dQ accumulator is cleared.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
@@ -666,7 +662,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       const long long row = row0 + k;
       if (lane == 0 && row < rows) {
         a.ddot[row] = valid[k] ? dsum : 0.f;
-        a.lse2[row] = valid[k] ? a.lse[lrow[k]] * kLog2e : INFINITY;
+        a.lse2[row] = valid[k] ? -(a.lse[lrow[k]] * kLog2e) : -INFINITY;
       }
     }
   }

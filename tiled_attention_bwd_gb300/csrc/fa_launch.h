@@ -35,7 +35,7 @@ struct BwdArgs {
   const float* lse;           // [BH, N]
   float* dq_acc;              // [BH, N, d]  fp32 workspace
   float* ddot;                // [BH, N_pad] D_i = dO_i . O_i  (0 past N)
-  float* lse2;                // [BH, N_pad] LSE_i * log2(e)   (+inf past N)
+  float* lse2;                // [BH, N_pad] -LSE_i * log2(e)  (-inf past N)
   __nv_bfloat16* dq;          // [BH, N, d]
   __nv_bfloat16* dk;          // [BHkv, N, d]
   __nv_bfloat16* dv;          // [BHkv, N, d]

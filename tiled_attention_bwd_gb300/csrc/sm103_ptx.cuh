@@ -281,6 +281,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Registers -> TMEM, 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+      "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -334,6 +344,30 @@ __device__ __forceinline__ void add2_acc(float& d0, float& d1, float a0,
       "mov.b64 {%0, %1}, t;\n\t}"
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
+}
+// (d0, d1) = (a0, a1) * (b, b) + (c0, c1)
+__device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1,
+                                        uint64_t b2, float c0, float c1) {
+  asm("{\n\t.reg .b64 t, u;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "mov.b64 u, {%5, %6};\n\t"
+      "fma.rn.f32x2 t, t, %4, u;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b2), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (a0, a1) * ((b0, b1) - (c0, c1))
+__device__ __forceinline__ void mulsub2(float& d0, float& d1, float a0, float a1,
+                                        float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 y, {%6, %7};\n\t"
+      "sub.rn.f32x2 y, x, y;\n\t"
+      "mov.b64 z, {%2, %3};\n\t"
+      "mul.rn.f32x2 y, z, y;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 // Both halves of a packed pair set to x.
 __device__ __forceinline__ uint64_t bcast2(float x) {
