@@ -1,7 +1,7 @@
 """Benchmark: attention forward + backward TFLOP/s on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--hkv HKV] [--window W] [--fp8]
+                    [--hkv HKV] [--window W] [--varlen] [--fp8]
                     [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
 
 One step = fa_fwd + fa_bwd over the whole workload (default: 4x64x4096x128
@@ -14,7 +14,9 @@ FLOP convention: forward = 4 B H N^2 d (halved when causal), backward = 2.5 x
 forward, step = 3.5 x forward.  With --window the N^2 (or N^2 / 2) becomes
 the number of visible (query, key) pairs of the band.  --hkv runs the
 grouped-query variant (K/V heads shared by H / HKV query heads); it does not
-change the FLOPs.
+change the FLOPs.  --varlen gives each batch entry its own length, drawn
+uniformly from [1, N] (seeded), through fa_fwd_varlen / fa_bwd_varlen; the
+FLOPs then count each sequence's own visible pairs.
 
 --impl reference times the CPU fp64 oracle (the plain definition, no tuning)
 on the host cores, each step a bounded sample of the same workload (the last
@@ -184,13 +186,24 @@ def oracle_sample(w, heads, rows, window=-1):
     return flops, dt
 
 
-def step_flops(w, window):
-    """Algorithmic FLOPs of one forward (and of one backward = 2.5 x)."""
+def step_flops(w, window, lens=None):
+    """Algorithmic FLOPs of one forward (and of one backward = 2.5 x); with
+    per-sequence lengths, each batch entry counts its own visible pairs."""
     from tiled_attention_bwd_gb300.workloads import visible_pairs
+    if lens is not None:
+        pairs = sum(visible_pairs(int(L), w.causal, window) for L in lens)
+        f = 4.0 * w.H * w.d * pairs
+        return f, 2.5 * f
     if window < 0:
         return w.fwd_flops(), w.bwd_flops()
     f = 4.0 * w.B * w.H * w.d * visible_pairs(w.N, w.causal, window)
     return f, 2.5 * f
+
+
+def bench_lengths(w):
+    """Per-sequence lengths of --varlen: uniform over [1, N], seeded."""
+    from tiled_attention_bwd_gb300.workloads import make_seq_lens
+    return make_seq_lens(w.B, w.N, seed=w.seed)
 
 
 def variant_config(w, args):
@@ -200,6 +213,9 @@ def variant_config(w, args):
         c["Hkv"] = args.hkv
     if args.window >= 0:
         c["window"] = args.window
+    if args.varlen:
+        c["seq_lens"] = [int(x) for x in bench_lengths(w)]
+        c["seq_lens_recipe"] = "uniform over [1, N], seed = workload seed"
     return c
 
 
@@ -241,8 +257,9 @@ def run_ours(args, w, rank, world, local):
     import torch
     from tiled_attention_bwd_gb300 import (fa_bwd_ext, fa_bwd_set_phase_events,
                                            fa_bwd_ext_workspace_size,
+                                           fa_bwd_varlen,
                                            fa_check_device_status, fa_fwd_ext,
-                                           load_library)
+                                           fa_fwd_varlen, load_library)
     from tiled_attention_bwd_gb300.workloads import make_grouped_inputs
 
     load_library()
@@ -263,15 +280,25 @@ def run_ours(args, w, rank, world, local):
     ws = torch.empty(fa_bwd_ext_workspace_size(w.B, w.H, hkv, w.N, w.d),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    fwd_flops, bwd_flops = step_flops(w, window)
+    lens_cpu = bench_lengths(w) if args.varlen else None
+    sl = lens_cpu.to(dev) if args.varlen else None
+    fwd_flops, bwd_flops = step_flops(w, window, lens_cpu)
 
     def fwd():
-        fa_fwd_ext(q, k, v, w.causal, w.scale, window, out=o, lse=lse)
+        if sl is None:
+            fa_fwd_ext(q, k, v, w.causal, w.scale, window, out=o, lse=lse)
+        else:
+            fa_fwd_varlen(q, k, v, sl, w.causal, w.scale, window, out=o,
+                          lse=lse)
 
     def step():
         fwd()
-        fa_bwd_ext(q, k, v, o, lse, do, w.causal, w.scale, window, dq=dq,
-                   dk=dk, dv=dv, workspace=ws)
+        if sl is None:
+            fa_bwd_ext(q, k, v, o, lse, do, w.causal, w.scale, window, dq=dq,
+                       dk=dk, dv=dv, workspace=ws)
+        else:
+            fa_bwd_varlen(q, k, v, o, lse, do, sl, w.causal, w.scale, window,
+                          dq=dq, dk=dk, dv=dv, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -355,13 +382,17 @@ def run_ours(args, w, rank, world, local):
                 for n in ("o", "dq", "dk", "dv")}
         lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
 
+        if sl is not None:
+            host["seq_lens"] = lens_cpu.pin_memory()
         if variant_config(w, args):
-            # grouped heads / window: copies and compute one after another
-            mode = "serial copies around fa_fwd_ext + fa_bwd_ext"
+            # grouped heads / window / lengths: copies and compute in turn
+            mode = "serial copies around the fa_*_ext or fa_*_varlen calls"
 
             def e2e_step():
                 for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
                     t.copy_(host[n], non_blocking=True)
+                if sl is not None:
+                    sl.copy_(host["seq_lens"], non_blocking=True)
                 step()
                 for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
                     outs[n].copy_(t, non_blocking=True)
@@ -470,6 +501,8 @@ def main():
                     help="sliding window |i - j| <= W (default: none)")
     ap.add_argument("--chunk-heads", type=int, default=0,
                     help="heads per chunk of the host-buffer step (0: B*H/16)")
+    ap.add_argument("--varlen", action="store_true",
+                    help="per-sequence lengths, uniform over [1, N]")
     ap.add_argument("--fp8", action="store_true",
                     help="also time the FP8 forward (fa_fwd_fp8)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -481,6 +514,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.hkv is not None and (args.hkv < 1 or w.H % args.hkv != 0):
         raise SystemExit("--hkv must divide H = %d" % w.H)
+    if args.varlen and args.fp8:
+        raise SystemExit("--varlen has no FP8 forward")
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, w, rank, world)

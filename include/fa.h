@@ -143,6 +143,36 @@ fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
                      void* stream);
 
 /*
+ * Per-sequence lengths over a padded batch: the "variable sequence lengths"
+ * that "GPU Performance Optimization Batch 1 -- Design Spec", Item 1 ("CUDA
+ * Graphs", Constraint) names as the product of dynamic padding.  Same
+ * operation, arguments and workspace as fa_fwd_ext / fa_bwd_ext, plus
+ *   - seq_lens: device int32 [B], 4-byte aligned, owned by the caller and
+ *     read by the kernels on `stream` (it may change between calls, or
+ *     between replays of a captured graph, without changing any shape).
+ *     Batch entry b is the plain operation on its first L_b = seq_lens[b]
+ *     rows of q, k, v, o, dout (every head of the entry): queries i < L_b
+ *     see keys j < L_b only, with the causal and window rules on top.
+ *     Lengths are clamped to [0, N]; L_b = 0 is an empty sequence.
+ *   - Rows at or past L_b are padding.  Their q, k, v, dout must be finite
+ *     (they multiply exact zeros); fa_fwd_varlen leaves o and lse there
+ *     unwritten; fa_bwd_varlen sets dq, dk, dv there to zero and never reads
+ *     o or lse there.
+ *   - seq_lens NULL or misaligned (with B > 0): FA_ERR_INVALID_ARG.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o,
+                        float* lse, const int* seq_lens, int B, int H, int Hkv,
+                        int N, int d, int causal, int window, float scale,
+                        void* stream);
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv, const int* seq_lens,
+                        void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int N, int d, int causal, int window,
+                        float scale, void* stream);
+
+/*
  * FP8 forward: the optional FP8 path of "GPU Performance Optimization Batch
  * 1 -- Design Spec", Item 3 ("FlashAttention-3 Blackwell"): before the
  * Q K^T product, Q and K are quantised to E4M3 block by block, each block

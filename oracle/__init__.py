@@ -26,6 +26,11 @@ What each function follows:
                  |i - j| <= window, and j <= i when causal).  The pages list
                  both as future variants ("Advanced Features (Future)":
                  multi-query / grouped query attention; sliding window).
+  fwd_varlen, bwd_varlen -- per-sequence lengths over a padded batch (the
+                 "variable sequence lengths" of "GPU Performance Optimization
+                 Batch 1 -- Design Spec", Item 1, Constraint): batch entry b
+                 is fwd_ext / bwd_ext on its first seq_lens[b] rows alone;
+                 the forward's padding rows are NaN, the gradients' zero.
   fp8         -- (submodule) E4M3 quantisation of Q and K per 16-row block
                  with one float32 scale each, and the forward on the
                  dequantised values ("GPU Performance Optimization Batch 1 --
@@ -223,3 +228,44 @@ def bwd_ext(q, k, v, dout, causal: bool, scale: float, window: int = -1,
                                 _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
+
+def _lengths(seq_lens, B, N):
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    if len(lens) != B:
+        raise ValueError("seq_lens has %d entries for B = %d" % (len(lens), B))
+    return [min(max(x, 0), N) for x in lens]
+
+
+def fwd_varlen(q, k, v, seq_lens, causal: bool, scale: float,
+               window: int = -1):
+    """Forward over a padded batch: entry b is fwd_ext on rows [0, L_b) of
+    its q, k, v (L_b = seq_lens[b] clamped to [0, N]).  O and LSE rows at or
+    past L_b are NaN."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, Hkv, N, d = _ext_shapes(q, k)
+    o = np.full_like(q, np.nan)
+    lse = np.full(q.shape[:-1], np.nan, dtype=np.float64)
+    for b, L in enumerate(_lengths(seq_lens, B, N)):
+        if L == 0:
+            continue
+        ob, lb = fwd_ext(q[b:b + 1, :, :L], k[b:b + 1, :, :L],
+                         v[b:b + 1, :, :L], causal, scale, window)
+        o[b, :, :L] = ob[0]
+        lse[b, :, :L] = lb[0]
+    return o, lse
+
+
+def bwd_varlen(q, k, v, dout, seq_lens, causal: bool, scale: float,
+               window: int = -1):
+    """Backward of fwd_varlen: entry b is bwd_ext on rows [0, L_b); the
+    gradients' rows at or past L_b are zero (padding does not take part)."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, H, Hkv, N, d = _ext_shapes(q, k)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(k)
+    for b, L in enumerate(_lengths(seq_lens, B, N)):
+        if L == 0:
+            continue
+        g = bwd_ext(q[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L],
+                    dout[b:b + 1, :, :L], causal, scale, window)
+        dq[b, :, :L], dk[b, :, :L], dv[b, :, :L] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

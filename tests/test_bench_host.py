@@ -104,3 +104,24 @@ def test_reference_arm_runs_with_a_window():
     line = json.loads(out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"]["window"] == 100 and line["config"]["Hkv"] == 2
+
+
+def test_step_flops_with_sequence_lengths():
+    from tiled_attention_bwd_gb300.workloads import WORKLOADS
+    w = WORKLOADS["xl_4x64x4096x128_causal"]
+    # each sequence counts its own visible pairs, L (L + 1) / 2 when causal
+    # (full lengths: within 1 / N of the N^2 / 2 convention of the plain run)
+    full = [w.N] * w.B
+    f, _ = bench.step_flops(w, -1, full)
+    assert f == pytest.approx(w.fwd_flops() * (1 + 1 / w.N))
+    lens = [4096, 1, 0, 129]
+    f, b = bench.step_flops(w, -1, lens)
+    pairs = sum(L * (L + 1) // 2 for L in lens)
+    assert f == 4.0 * w.H * w.d * pairs and b == 2.5 * f
+    f, _ = bench.step_flops(w, 16, [40])
+    band = sum(min(i, 16) + 1 for i in range(40))     # causal band of 17
+    assert f == 4.0 * w.H * w.d * band
+    drawn = bench.bench_lengths(w)
+    assert drawn.dtype.is_floating_point is False and len(drawn) == w.B
+    assert all(1 <= int(x) <= w.N for x in drawn)
+    assert bench.bench_lengths(w).tolist() == drawn.tolist()    # seeded

@@ -26,6 +26,7 @@ def test_header_declares_the_expected_entry_points():
     names = fa.header_functions()
     for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
               "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_ext_workspace_size",
+              "fa_fwd_varlen", "fa_bwd_varlen",
               "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_quantize_e4m3",
               "fa_check_device_status", "fa_status_string",
               "fa_set_wait_timeout_ns", "fa_debug_expire_wait"):
@@ -188,6 +189,52 @@ def test_python_binding_checks_grouped_shapes():
         fa._check_ext_shapes(q, k)     # sequence lengths differ
     k = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16)
     assert fa._check_ext_shapes(q, k) == (1, 4, 2, 8, 64)
+
+
+def _fwd_varlen(lib, ptr=16, lse=16, sl=16, B=2, H=4, Hkv=2, N=128, d=128,
+                causal=0, window=-1, scale=0.125):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_fwd_varlen(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), p(sl), B,
+                             H, Hkv, N, d, causal, window, scale, None)
+
+
+def _bwd_varlen(lib, ptr=16, ws=16, ws_bytes=1 << 40, sl=16, B=2, H=4, Hkv=2,
+                N=128, d=128, causal=0, window=-1, scale=0.125, lse=16):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_bwd_varlen(p(ptr), p(ptr), p(ptr), p(ptr), p(lse), p(ptr),
+                             p(ptr), p(ptr), p(ptr), p(sl), p(ws), ws_bytes, B,
+                             H, Hkv, N, d, causal, window, scale, None)
+
+
+def test_varlen_argument_checks(lib):
+    for call in (_fwd_varlen, _bwd_varlen):
+        assert call(lib, sl=0) == INVALID          # lengths are required
+        assert call(lib, sl=18) == INVALID         # not 4-byte aligned
+        assert call(lib, ptr=0) == INVALID
+        assert call(lib, H=4, Hkv=3) == INVALID
+        assert call(lib, scale=0.0) == INVALID
+        assert call(lib, d=96) == UNSUPPORTED
+        # Empty problems are no-ops; with B = 0 there are no lengths to read.
+        assert call(lib, ptr=0, lse=0, sl=0, B=0) == OK
+        assert call(lib, ptr=0, lse=0, N=0) == OK
+    assert _bwd_varlen(lib, ws=0) == WORKSPACE
+    need = lib.fa_bwd_ext_workspace_size(2, 4, 2, 128, 128)
+    assert _bwd_varlen(lib, ws_bytes=need - 1) == WORKSPACE
+
+
+def test_python_binding_checks_seq_lens():
+    import torch
+    good = torch.zeros(3, dtype=torch.int32)
+    fa._check_seq_lens(good, 3, good.device)
+    for bad in (torch.zeros(3, dtype=torch.int64),      # wrong dtype
+                torch.zeros(4, dtype=torch.int32),      # wrong length
+                torch.zeros((3, 1), dtype=torch.int32),
+                torch.zeros(6, dtype=torch.int32)[::2],  # not contiguous
+                [1, 2, 3]):                              # not a tensor
+        with pytest.raises(ValueError):
+            fa._check_seq_lens(bad, 3, good.device)
+    with pytest.raises(ValueError):
+        fa._check_seq_lens(good, 3, torch.device("meta"))
 
 
 def _fwd_fp8(lib, ptr=256, lse=16, ws=256, ws_bytes=1 << 40, B=1, H=1, N=128,

@@ -253,9 +253,14 @@ void fa_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
 }
 
-fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
-                     float* lse, int B, int H, int Hkv, int N, int d,
-                     int causal, int window, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
+                   float* lse, const int* seq_lens, int B, int H, int Hkv,
+                   int N, int d, int causal, int window, float scale,
+                   void* stream) {
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
   if (s != FA_OK) return s;
@@ -279,7 +284,10 @@ fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
   a.N = N;
   a.H = H;
   a.Hkv = Hkv;
-  a.window = win;
+  // Only the windowed forward kernels read per-sequence lengths; a window
+  // of N - 1 hides no key, so a call with lengths and no window runs there.
+  a.window = (seq_lens && win < 0) ? N - 1 : win;
+  a.seq_lens = seq_lens;
   a.group = BH;  // the forward schedules over all heads at once
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
@@ -289,10 +297,31 @@ fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_ext(const void* q, const void* k, const void* v, void* o,
+                     float* lse, int B, int H, int Hkv, int N, int d,
+                     int causal, int window, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, nullptr, B, H, Hkv, N, d, causal, window,
+                  scale, stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o,
+                        float* lse, const int* seq_lens, int B, int H, int Hkv,
+                        int N, int d, int causal, int window, float scale,
+                        void* stream) {
+  if (B > 0 && (!seq_lens || !aligned(seq_lens, 4))) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, seq_lens, B, H, Hkv, N, d, causal, window,
+                  scale, stream);
+}
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
                  float* lse, int B, int H, int N, int d, int causal,
                  float scale, void* stream) {
-  return fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, causal, -1, scale, stream);
+  return fwd_impl(q, k, v, o, lse, nullptr, B, H, H, N, d, causal, -1, scale,
+                  stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -309,12 +338,16 @@ size_t fa_bwd_ext_workspace_size(int B, int H, int Hkv, int N, int d) {
   return ws_layout(B, H, Hkv, N, d).total;
 }
 
-fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
-                     const void* o, const float* lse, const void* dout,
-                     void* dq, void* dk, void* dv, void* workspace,
-                     size_t workspace_bytes, int B, int H, int Hkv, int N,
-                     int d, int causal, int window, float scale,
-                     void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status bwd_impl(const void* q, const void* k, const void* v,
+                   const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, const int* seq_lens,
+                   void* workspace, size_t workspace_bytes, int B, int H,
+                   int Hkv, int N, int d, int causal, int window, float scale,
+                   void* stream) {
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
   if (s != FA_OK) return s;
@@ -353,6 +386,7 @@ fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
   a.dv_acc = reinterpret_cast<float*>(ws + w.dv_acc_off);
   a.hpb = w.hpb;
   a.nsplit = w.nsplit;
+  a.seq_lens = seq_lens;
   a.BH = BH;
   a.BHkv = BHkv;
   a.H = H;
@@ -381,12 +415,39 @@ fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_ext(const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N,
+                     int d, int causal, int window, float scale,
+                     void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, nullptr, workspace,
+                  workspace_bytes, B, H, Hkv, N, d, causal, window, scale,
+                  stream);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv, const int* seq_lens,
+                        void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int N, int d, int causal, int window,
+                        float scale, void* stream) {
+  if (B > 0 && (!seq_lens || !aligned(seq_lens, 4))) return FA_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, seq_lens, workspace,
+                  workspace_bytes, B, H, Hkv, N, d, causal, window, scale,
+                  stream);
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dout, void* dq, void* dk,
                  void* dv, void* workspace, size_t workspace_bytes, int B,
                  int H, int N, int d, int causal, float scale, void* stream) {
-  return fa_bwd_ext(q, k, v, o, lse, dout, dq, dk, dv, workspace,
-                    workspace_bytes, B, H, H, N, d, causal, -1, scale, stream);
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, nullptr, workspace,
+                  workspace_bytes, B, H, H, N, d, causal, -1, scale, stream);
 }
 
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {

@@ -111,11 +111,12 @@ enum : uint32_t {
 // column `tcol` (this thread's lane), times `mul`: rounded to bf16 into `out`,
 // or, when the group's query heads are split over several blocks, added in
 // fp32 into `acc` (vector atomics; rounded later by the post kernel).
+// Rows at or past `len` (the sequence's length) are not written.
 template <int D>
 __device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
                                             float* acc, int bkv, int krow,
-                                            int N, float mul) {
-  const bool valid = krow < N;
+                                            int N, int len, float mul) {
+  const bool valid = krow < len;
   const size_t row = (size_t)bkv * N + (valid ? krow : 0);
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
@@ -147,7 +148,7 @@ __device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -183,18 +184,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int j = slot.tile;                        // key tile
   const int qgroup = a.H / a.Hkv;
   const int qh0 = (bkv / a.Hkv) * a.H + (bkv % a.Hkv) * qgroup + split * a.hpb;
+  // With per-sequence lengths (the VARLEN instantiations; the others keep
+  // none of this arithmetic) only the sequence's own tiles count: a key tile
+  // at or past its end gives the block no work (nq = 0).
+  const int len = VARLEN ? seq_len_of(a.seq_lens, bkv / a.Hkv, a.N) : a.N;
+  const int tiles_b = VARLEN ? (len + kTile - 1) / kTile : n_tiles;
   int i_lo, i_hi;
   {
     const long long k0 = (long long)j * kTile, k1 = k0 + kTile - 1;
     i_lo = CAUSAL ? j : ((a.window >= 0 && k0 > a.window)
                              ? (int)((k0 - a.window) / kTile) : 0);
-    i_hi = n_tiles - 1;
+    i_hi = tiles_b - 1;
     if (a.window >= 0) {
       const long long h = (k1 + a.window) / kTile;
       if (h < i_hi) i_hi = (int)h;
     }
   }
-  const int nq = a.hpb * (i_hi - i_lo + 1);
+  const int nq = (!VARLEN || (j < tiles_b && i_hi >= i_lo))
+                     ? a.hpb * (i_hi - i_lo + 1) : 0;
+  // A block with no work (a key tile past its sequence's end) leaves before
+  // any barrier, TMEM or shared-memory setup: with short sequences most
+  // blocks of the grid are such blocks.  The condition is uniform over the
+  // block and nothing has been issued yet.
+  if (VARLEN && nq == 0) return;
   // Walks (query head, query tile) in iteration order without divisions.
   struct QCursor {
     int bh, i;
@@ -421,6 +433,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // INT_MAX: no bound); a tile pair needs the mask only if its offsets
     // reach outside [dmin, dmax].  Tile offsets fit in int because
     // N <= 2^30 and the window is below N.
+    // With per-sequence lengths, key rows past the sequence's end hold real
+    // (finite) data, so their P must be forced to zero: the tile that holds
+    // the end takes the masked path, with no visible query for those rows.
+    const bool key_in = j * kTile + r < len;
+    const bool tail = VARLEN && (j + 1) * kTile > len;
     const int win = a.window;
     const int dmin = CAUSAL ? 0 : (win >= 0 ? -win : INT_MIN);
     const int dmax = win >= 0 ? win : INT_MAX;
@@ -445,7 +462,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // over S columns that have already been read.
       uint32_t pk[64];
       const int off0 = (i - j) * kTile;  // q - k where local q = local k
-      const bool edge = (dmin != INT_MIN && off0 - (kTile - 1) < dmin) ||
+      const bool edge = tail ||
+                        (dmin != INT_MIN && off0 - (kTile - 1) < dmin) ||
                         (dmax != INT_MAX && off0 + (kTile - 1) > dmax);
       // Local query index q is visible to key row r when q_lo <= q <= q_hi.
       int q_lo = 0, q_hi = kTile - 1;
@@ -455,6 +473,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           q_lo = (int)max(0ll, min((long long)kTile, dmin - base));
         if (dmax != INT_MAX)
           q_hi = (int)max(-1ll, min((long long)kTile - 1, dmax - base));
+        if (VARLEN && !key_in) q_lo = kTile;
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -542,7 +561,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       tc_fence_after();
       kv_epilogue<D>(tl + 256, a.dk, a.nsplit > 1 ? a.dk_acc : nullptr, bkv,
-                     j * kTile + r, a.N, a.scale);
+                     j * kTile + r, a.N, len, a.scale);
     }
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
@@ -601,7 +620,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       tc_fence_after();
       kv_epilogue<D>(tl + 256 + D, a.dv, a.nsplit > 1 ? a.dv_acc : nullptr,
-                     bkv, j * kTile + r, a.N, 1.0f);
+                     bkv, j * kTile + r, a.N, len, 1.0f);
     }
   }
 
@@ -633,7 +652,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       const long long row = row0 + k;
       const int bh = (int)(row / a.N_pad);
       const int q = (int)(row - (long long)bh * a.N_pad);
-      valid[k] = row < rows && q < a.N;
+      valid[k] = row < rows &&
+                 q < (a.seq_lens ? seq_len_of(a.seq_lens, bh / a.H, a.N) : a.N);
       lrow[k] = (long long)bh * a.N + q;
 #pragma unroll
       for (int e = 0; e < kPer / 2; ++e) ov[k][e] = dv[k][e] = 0u;
@@ -698,8 +718,30 @@ __device__ __forceinline__ void round_rows(const float* acc_f, __nv_bfloat16* ou
   }
 }
 
+// Rows at or past their sequence's end -> 0 in a [heads_total, N, d] bf16
+// tensor whose batch entry is head / heads (eight elements per step).
+__device__ __forceinline__ void zero_tail_rows(__nv_bfloat16* out_b,
+                                               long long heads_total, int heads,
+                                               int N, int d,
+                                               const int* seq_lens) {
+  uint4* out = reinterpret_cast<uint4*>(out_b);
+  const int per_row = d / 8;
+  const long long n8 = heads_total * N * per_row;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long row = idx / per_row;
+    const long long h = row / N;
+    const int q = (int)(row - h * N);
+    if (q >= seq_len_of(seq_lens, (int)(h / heads), N))
+      out[idx] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // dQ = scale * accumulator -> bf16, eight elements per thread per step; with
-// split key/value groups also dK and dV (already scaled) -> bf16.
+// split key/value groups also dK and dV (already scaled) -> bf16.  With
+// per-sequence lengths the rows past each sequence's end of dQ, dK and dV
+// are then set to zero (the same thread rewrites the same elements, so the
+// zeros land last).
 __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
   round_rows(a.dq_acc, a.dq, (long long)a.BH * a.N * d / 8, a.scale);
   if (a.nsplit > 1) {
@@ -707,15 +749,20 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
     round_rows(a.dk_acc, a.dk, m8, 1.0f);
     round_rows(a.dv_acc, a.dv, m8, 1.0f);
   }
+  if (a.seq_lens) {
+    zero_tail_rows(a.dq, a.BH, a.H, a.N, d, a.seq_lens);
+    zero_tail_rows(a.dk, a.BHkv, a.Hkv, a.N, d, a.seq_lens);
+    zero_tail_rows(a.dv, a.BHkv, a.Hkv, a.N, d, a.seq_lens);
+  }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdq, const BwdArgs& a,
                           cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto kern = bwd_main_kernel<D, CAUSAL>;
+  auto kern = bwd_main_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -740,11 +787,19 @@ cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdq, const BwdArgs& a, int d,
                             bool causal, cudaStream_t stream) {
-  if (d == 128)
-    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdq, a, stream)
-                  : launch_main_t<128, false>(tq, tk, tv, tdo, tdq, a, stream);
-  return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdq, a, stream)
-                : launch_main_t<64, false>(tq, tk, tv, tdo, tdq, a, stream);
+  const bool vl = a.seq_lens != nullptr;
+  if (d == 128) {
+    if (causal)
+      return vl ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tdq, a, stream)
+                : launch_main_t<128, true, false>(tq, tk, tv, tdo, tdq, a, stream);
+    return vl ? launch_main_t<128, false, true>(tq, tk, tv, tdo, tdq, a, stream)
+              : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdq, a, stream);
+  }
+  if (causal)
+    return vl ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tdq, a, stream)
+              : launch_main_t<64, true, false>(tq, tk, tv, tdo, tdq, a, stream);
+  return vl ? launch_main_t<64, false, true>(tq, tk, tv, tdo, tdq, a, stream)
+            : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,

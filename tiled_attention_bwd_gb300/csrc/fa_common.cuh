@@ -149,6 +149,15 @@ __device__ __forceinline__ TileSlot grouped_slot(int linear, int n_tiles,
 }
 
 // Aligns the dynamic shared memory base to 1024 bytes (128-byte swizzle atoms).
+// Length of batch entry b's sequence: N without per-sequence lengths, else
+// seq_lens[b] clamped to [0, N] (an out-of-range length cannot send a tile
+// past the tensor).
+__device__ __forceinline__ int seq_len_of(const int* seq_lens, int b, int N) {
+  if (!seq_lens) return N;
+  const int l = seq_lens[b];
+  return l < 0 ? 0 : (l > N ? N : l);
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   uintptr_t a = reinterpret_cast<uintptr_t>(p);
   return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));

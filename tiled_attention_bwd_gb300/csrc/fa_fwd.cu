@@ -75,6 +75,9 @@ struct FwdLayout {
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
 };
+// Bytes reserved for the barriers; the item table of the VARLEN kernels
+// follows them.
+constexpr int kFwdBarBytes = 256;
 
 template <int STAGES>
 struct FwdBars {
@@ -145,7 +148,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
 // Key tiles [lo, hi] that Q tile qt must visit.  Query i sees key j when
 // j <= i (causal) and |i - j| <= window (window >= 0); rows and keys past N
 // are handled by the masks.  `window` is below N here (a wider band is the
-// same as none and is passed as -1).
+// same as none and is passed as -1, or as N - 1 with per-sequence lengths).
 template <bool CAUSAL>
 __device__ __forceinline__ void key_range(int qt, int n_tiles, int window,
                                           int& lo, int& hi) {
@@ -167,25 +170,145 @@ __device__ __forceinline__ void key_range(int qt, int n_tiles, int window,
 // head: query head h of a batch entry reads head h / (H / Hkv).
 struct FwdItem {
   int bh, kvh, qt0, qt1, lo0, hi0, lo1, hi1, jb, je;
+  int len;  // rows of this batch entry's sequence (N without lengths)
 };
 // Items are ordered heaviest first over the whole grid (pair index slow,
 // head fast; causal pairs from the last one down).  Measured: grouping heads
 // so that their K/V stay in L2 cut DRAM reads but cost more in balance than
 // it saved, so the forward uses the global order.
+// Balanced item order with per-sequence lengths.  The plain order assumes
+// that every head has the same items; with lengths, items past a sequence's
+// end are empty and the dealing of the remaining ones to blocks loses its
+// balance.  So each block first builds, in shared memory, the same compact
+// list of non-empty items in decreasing cost:
+//   np[b]    pairs of Q tiles of sequence b (ceil(tiles / 2));
+//   order[s] sequences by decreasing np (ties by index: every block gets the
+//            same order, so the item lists agree);
+//   pref[x]  item counts before group x, where a group is a pair index from
+//            the last one down (causal: a pair's cost is the same for every
+//            sequence that has it, and the sequences that have pair p are the
+//            first ones of `order`) or a sequence in `order` (otherwise: a
+//            sequence's pairs all cost its length).
+// Returns the number of items.  All threads of the block take part.
 template <bool CAUSAL>
+__device__ int build_item_table(int* tab, const FwdArgs& a, int n_pairs) {
+  const int B = a.BH / a.H;
+  int* np = tab;
+  int* order = tab + B;
+  int* pref = tab + 2 * B;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int b = tid; b < B; b += nt) {
+    const int tiles = (seq_len_of(a.seq_lens, b, a.N) + kTile - 1) / kTile;
+    np[b] = (tiles + 1) / 2;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += nt) {
+    const int v = np[b];
+    int rank = 0;
+    for (int b2 = 0; b2 < B; ++b2) {
+      const int v2 = np[b2];
+      rank += (v2 > v) || (v2 == v && b2 < b);
+    }
+    order[rank] = b;
+  }
+  __syncthreads();
+  const int X = CAUSAL ? n_pairs : B;
+  for (int x = tid; x < X; x += nt) {
+    int cnt;
+    if (CAUSAL) {  // sequences with more than p pairs: a prefix of `order`
+      const int p = n_pairs - 1 - x;
+      int lo = 0, hi = B;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (np[order[mid]] > p) lo = mid + 1; else hi = mid;
+      }
+      cnt = lo;
+    } else {
+      cnt = np[order[x]];
+    }
+    pref[x + 1] = cnt * a.H;
+  }
+  __syncthreads();
+  if (tid < 32) {  // inclusive scan of pref[1..X]: one chunk per lane
+    const int chunk = (X + 31) / 32;
+    const int x0 = tid * chunk, x1 = min(X, x0 + chunk);
+    int sum = 0;
+    for (int x = x0; x < x1; ++x) sum += pref[x + 1];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += t;
+    }
+    int run = incl - sum;
+    for (int x = x0; x < x1; ++x) {
+      run += pref[x + 1];
+      pref[x + 1] = run;
+    }
+    if (tid == 0) pref[0] = 0;
+  }
+  __syncthreads();
+  return pref[X];
+}
+
+// Query head and pair index of compact item c (see build_item_table).
+template <bool CAUSAL>
+__device__ __forceinline__ void table_item(int c, const int* tab, int B,
+                                           int H, int n_pairs, int& bh,
+                                           int& pair) {
+  const int* order = tab + B;
+  const int* pref = tab + 2 * B;
+  int lo = 0, hi = (CAUSAL ? n_pairs : B) - 1;  // last group with pref <= c
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  const int k = c - pref[lo];
+  int s, h;
+  if (CAUSAL) {
+    pair = n_pairs - 1 - lo;
+    s = k / H;
+    h = k - s * H;
+  } else {
+    s = lo;
+    pair = k / H;
+    h = k - pair * H;
+  }
+  bh = order[s] * H + h;
+}
+
+// Per-sequence lengths are honoured by the VARLEN instantiations only, which
+// are windowed ones (the host runs a call with lengths and no window as one
+// with a window of N - 1, which hides nothing): in the other instantiations
+// the length's per-item arithmetic cost registers and about 5% of the time.
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
-                                            const FwdArgs& a) {
-  const int rank = w / a.BH;
-  const int pair = CAUSAL ? (n_pairs - 1 - rank) : rank;
+                                            const FwdArgs& a, const int* tab) {
   FwdItem it;
-  it.bh = w - rank * a.BH;
+  int pair;
+  if (VARLEN && tab) {
+    table_item<CAUSAL>(w, tab, a.BH / a.H, a.H, n_pairs, it.bh, pair);
+  } else {
+    const int rank = w / a.BH;
+    pair = CAUSAL ? (n_pairs - 1 - rank) : rank;
+    it.bh = w - rank * a.BH;
+  }
   const int b = it.bh / a.H, h = it.bh - b * a.H;
   it.kvh = b * a.Hkv + h / (a.H / a.Hkv);
   it.qt0 = 2 * pair;
   it.qt1 = 2 * pair + 1;
-  key_range<CAUSAL>(it.qt0, n_tiles, a.window, it.lo0, it.hi0);
-  if (it.qt1 < n_tiles) {
-    key_range<CAUSAL>(it.qt1, n_tiles, a.window, it.lo1, it.hi1);
+  // With per-sequence lengths, tiles at or past the sequence's end are not
+  // visited; an item with no tile left is empty (hi0 = -1) for every role.
+  it.len = VARLEN ? seq_len_of(a.seq_lens, b, a.N) : a.N;
+  const int tiles_b = VARLEN ? (it.len + kTile - 1) / kTile : n_tiles;
+  if (VARLEN && it.qt0 >= tiles_b) {
+    it.lo0 = it.lo1 = it.jb = 0;
+    it.hi0 = it.hi1 = it.je = -1;
+    return it;
+  }
+  key_range<CAUSAL>(it.qt0, tiles_b, a.window, it.lo0, it.hi0);
+  if (it.qt1 < tiles_b) {
+    key_range<CAUSAL>(it.qt1, tiles_b, a.window, it.lo1, it.hi1);
   } else {
     it.lo1 = 0;
     it.hi1 = -1;
@@ -207,7 +330,7 @@ __device__ __forceinline__ int fwd_round_item(int r) {
 // phases run on across items, so the producer fetches the next item's Q and
 // K/V while the current one finishes, and the next item's first Q K^T
 // overlaps the softmax warps' epilogue.
-template <int D, bool CAUSAL, bool WINDOW, bool FP8>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
@@ -219,6 +342,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   static_assert(!FP8 || D == 128, "the FP8 path needs d = 128");
   constexpr uint32_t kQKBytes = FP8 ? kTile * D : L::kTileBytes;
   constexpr int kQKBoxes = FP8 ? 1 : L::kSub;
+  static_assert(sizeof(FwdBars<S>) <= kFwdBarBytes, "barrier block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   auto* bars = reinterpret_cast<FwdBars<S>*>(smem + L::kBarOff);
@@ -226,7 +350,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const int n_pairs = (n_tiles + 1) / 2;
-  const int n_items = a.BH * n_pairs;
+  int n_items = a.BH * n_pairs;
+  const int* tab = nullptr;
+  if constexpr (VARLEN) {
+    if (a.sched) {
+      int* t = reinterpret_cast<int*>(smem + L::kBarOff + kFwdBarBytes);
+      n_items = build_item_table<CAUSAL>(t, a, n_pairs);
+      tab = t;
+    }
+  }
 
   if (threadIdx.x == 0) {
     bars->abort = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
@@ -273,7 +405,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
            w = fwd_round_item(++r)) {
-        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
+        const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
+        if (VARLEN && itm.hi0 < 0) continue;  // empty (past its sequence's end)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || (t == 1 && itm.hi1 < 0)) break;
@@ -360,7 +493,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
            w = fwd_round_item(++r)) {
-        const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
+        const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
+        if (VARLEN && itm.hi0 < 0) continue;  // empty item
         auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
         auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
         ok = wait_bar<kInl>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
@@ -432,7 +566,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = run;
     for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
          w = fwd_round_item(++r)) {
-      const FwdItem itm = fwd_item<CAUSAL>(w, n_tiles, n_pairs, a);
+      const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
       const int lo_t = t ? itm.lo1 : itm.lo0;
       const int hi_t = t ? itm.hi1 : itm.hi0;
       if (hi_t < 0) continue;
@@ -444,10 +578,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // if it reaches below the Q tile's largest lower bound or above its
       // smallest upper bound; the window is below N, so none of these sums
       // overflows.
-      const int win = a.window, nm1 = a.N - 1;
+      // Everything the masks need is derived here, once per item, so that
+      // the loop keeps as few values live as possible: without a window,
+      // the last tile's bound (uniform over the warp without causality);
+      // with one, the row's own visible key range.
+      const int win = a.window, nm1 = itm.len - 1;
       const int klo_max = WINDOW ? q0 + kTile - 1 - win : -1;
       const int khi_min =
           CAUSAL ? q0 : (WINDOW ? (q0 > nm1 - win ? nm1 : q0 + win) : nm1);
+      const int lim_last = (CAUSAL ? qrow : nm1) - hi_t * kTile;
+      const int row_lo = qrow > win ? qrow - win : 0;
+      const int row_hi = CAUSAL ? qrow : (qrow > nm1 - win ? nm1 : qrow + win);
       // FP8: scores are in units of sq(row block) * sk(key block); the row's
       // factor is folded into its exponent scale.
       float cr = c;
@@ -476,18 +617,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         reg_fence32(s + 64);
         reg_fence32(s + 96);
         if constexpr (!WINDOW) {
-          if (j == hi_t && (CAUSAL || (a.N & (kTile - 1)))) {
-            const int lim = (CAUSAL ? qrow : nm1) - j * kTile;
+          if (j == hi_t && (CAUSAL || lim_last < kTile - 1)) {
 #pragma unroll
             for (int e = 0; e < 128; ++e)
-              if (e > lim) s[e] = __float_as_uint(-INFINITY);
+              if (e > lim_last) s[e] = __float_as_uint(-INFINITY);
           }
         } else {
           const int kb = j * kTile;
           if (kb < klo_max || kb + kTile - 1 > khi_min) {
-            const int row_lo = qrow > win ? qrow - win : 0;
-            const int row_hi =
-                CAUSAL ? qrow : (qrow > nm1 - win ? nm1 : qrow + win);
             const int e_lo = row_lo - kb, e_hi = row_hi - kb;
 #pragma unroll
             for (int e = 0; e < 128; ++e)
@@ -588,7 +725,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const bool valid = qrow < a.N;
+      // The length is read again rather than kept live through the loop.
+      const bool valid =
+          qrow < (VARLEN ? seq_len_of(a.seq_lens, itm.bh / a.H, a.N) : a.N);
       __nv_bfloat16* orow = a.o + ((size_t)itm.bh * a.N + (valid ? qrow : 0)) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -625,12 +764,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool WINDOW, bool FP8>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8>;
+  static_assert(!VARLEN || (WINDOW && !FP8), "lengths run windowed, bf16");
+  auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8, VARLEN>;
   cudaError_t e;
   if constexpr (kSplitRegs) {
     // The register split inside the kernel assumes exactly kLaunchRegs per
@@ -641,13 +781,34 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     if (fa_attr.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   }
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int n_items = BH * ((n_tiles + 1) / 2);
+  const int n_pairs = (n_tiles + 1) / 2;
+  FwdArgs args = a;
+  size_t smem_bytes = L::kSmemBytes;
+  args.sched = 0;
+  if constexpr (VARLEN) {
+    // The balanced item table (np, order: B ints each; pref: groups + 1)
+    // when it fits in the shared memory left by the tiles.
+    const long long B = a.BH / a.H;
+    const long long groups = CAUSAL ? n_pairs : B;
+    const long long table = 4 * (2 * B + groups + 1);
+    int dev = 0, optin = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&optin,
+                                 cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if ((long long)L::kSmemBytes + table <= optin) {
+      smem_bytes = L::kSmemBytes + (size_t)table;
+      args.sched = 1;
+    }
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes);
+  if (e != cudaSuccess) return e;
+  const int n_items = BH * n_pairs;
   const int blocks = n_items < grid_blocks ? n_items : grid_blocks;
-  kern<<<blocks, kFwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, a);
+  kern<<<blocks, kFwdThreads, smem_bytes, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
@@ -655,6 +816,10 @@ template <int D, bool CAUSAL>
 cudaError_t launch_fwd_w(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
+  if (a.seq_lens)  // the host passes a window (N - 1 at widest) with lengths
+    return a.window >= 0
+               ? launch_fwd_t<D, CAUSAL, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+               : cudaErrorInvalidValue;
   return a.window >= 0
              ? launch_fwd_t<D, CAUSAL, true, false>(tq, tk, tv, a, BH, grid_blocks, stream)
              : launch_fwd_t<D, CAUSAL, false, false>(tq, tk, tv, a, BH, grid_blocks, stream);

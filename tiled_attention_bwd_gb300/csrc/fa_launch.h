@@ -20,6 +20,12 @@ struct FwdArgs {
   int window;           // band half-width in keys, < 0: none
   int group;            // heads per scheduling group
   float scale_log2;     // scale * log2(e): scores enter exp2 directly
+  // Per-sequence lengths ([B] int32, device) or null: batch entry b attends
+  // over its first seq_lens[b] rows only.
+  const int* seq_lens;
+  // With lengths: 1 when the kernel builds its balanced item table in shared
+  // memory (set by the launcher when the table fits), else 0.
+  int sched;
   // FP8 path only: per-16-row-block scales of the E4M3 Q and K,
   // [BH or BHkv][n_sblk] with n_sblk = N rounded up to 128, over 16.
   const float* q_scale;
@@ -46,6 +52,7 @@ struct BwdArgs {
   int H;                      // query heads per batch entry
   int Hkv;                    // key/value heads per batch entry (divides H)
   int window;                 // band half-width in keys, < 0: none
+  const int* seq_lens;        // [B] int32 per-sequence lengths, or null
   int hpb;                    // query heads per block (divides H / Hkv)
   int nsplit;                 // blocks per (key/value head, key tile)
   int N;

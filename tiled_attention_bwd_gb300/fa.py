@@ -66,6 +66,12 @@ def open_library(path: str):
     lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
     lib.fa_bwd_ext.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                  i, f, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                  ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
+    lib.fa_bwd_varlen.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                i, i, i, i, i, f, vp]
     lib.fa_fwd_fp8.restype = i
@@ -289,6 +295,80 @@ def fa_bwd_ext(q, k, v, o, lse, dout, causal: bool, scale: float,
         _check("fa_bwd_ext", lib.fa_bwd_ext(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+            int(bool(causal)), int(window), float(scale),
+            _stream_handle(q.device)))
+    return dq, dk, dv
+
+
+def _check_seq_lens(seq_lens, B, device):
+    if not isinstance(seq_lens, torch.Tensor) or seq_lens.dtype != torch.int32 \
+            or tuple(seq_lens.shape) != (B,) or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 tensor [B] = [%d]"
+                         % B)
+    if seq_lens.device != device:
+        raise ValueError("seq_lens is on %s, the inputs on %s"
+                         % (seq_lens.device, device))
+
+
+def fa_fwd_varlen(q, k, v, seq_lens, causal: bool, scale: float,
+                  window: int = -1, out=None, lse=None):
+    """fa_fwd_ext over a padded batch: batch entry b attends over its first
+    seq_lens[b] rows only (int32 [B] on the inputs' device, clamped to
+    [0, N]).  Rows past a sequence's end of the returned O and LSE are left
+    as they were (unwritten).  Returns (O, LSE)."""
+    lib = load_library()
+    B, H, Hkv, N, d = _check_ext_shapes(q, k)
+    _check_qkv("q", q)
+    _check_qkv("k", k, (B, Hkv, N, d))
+    _check_qkv("v", v, (B, Hkv, N, d))
+    _check_seq_lens(seq_lens, B, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_qkv("out", out, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    with torch.cuda.device(q.device):
+        _check("fa_fwd_varlen", lib.fa_fwd_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seq_lens),
+            B, H, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+            _stream_handle(q.device)))
+    return out, lse
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, seq_lens, causal: bool,
+                  scale: float, window: int = -1, dq=None, dk=None, dv=None,
+                  workspace=None):
+    """Backward of fa_fwd_varlen.  Returns (dQ [B,H,N,d], dK, dV [B,Hkv,N,d])
+    with every row past its sequence's end set to zero."""
+    lib = load_library()
+    B, H, Hkv, N, d = _check_ext_shapes(q, k)
+    _check_qkv("q", q)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    for name, t in (("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    _check_seq_lens(seq_lens, B, q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_qkv("dq", dq, q.shape)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    need = fa_bwd_ext_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=q.device)
+    with torch.cuda.device(q.device):
+        _check("fa_bwd_varlen", lib.fa_bwd_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(seq_lens), _ptr(workspace),
             workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
             int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))

@@ -102,6 +102,16 @@ def make_grouped_inputs(B: int, H: int, Hkv: int, N: int, d: int, seed: int,
     return out
 
 
+def make_seq_lens(B: int, N: int, seed: int, fixed=()):
+    """int32 [B] per-sequence lengths: the leading entries are `fixed`
+    (clamped to [0, N]), the rest drawn uniformly from [1, N]."""
+    rng = np.random.default_rng(int(seed))
+    lens = [min(max(int(x), 0), N) for x in fixed][:B]
+    if len(lens) < B:
+        lens += [int(x) for x in rng.integers(1, N + 1, B - len(lens))]
+    return torch.tensor(lens, dtype=torch.int32)
+
+
 def visible_pairs(N: int, causal: bool, window: int, r0: int = 0,
                   r1: int = None) -> int:
     """Number of (query, key) pairs with the query in rows [r0, r1) that a
