@@ -633,6 +633,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// Per-sequence lengths: work on a [heads_total, N, *] tensor in units of
+// kChunkRows rows of one head, dealt over the grid's blocks; f(h, r0, r1, len)
+// handles rows [r0, r1) of head h, whose sequence (batch entry h / heads)
+// has length len.  One division per unit instead of one per row keeps these
+// HBM-bound loops from being instruction-bound.
+constexpr int kChunkRows = 64;
+template <class F>
+__device__ __forceinline__ void over_row_chunks(long long heads_total, int heads,
+                                                int N, const int* seq_lens,
+                                                F&& f) {
+  const int chunks = (N + kChunkRows - 1) / kChunkRows;
+  const long long units = heads_total * chunks;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const long long h = u / chunks;
+    const int r0 = (int)(u - h * chunks) * kChunkRows;
+    const int r1 = r0 + kChunkRows < N ? r0 + kChunkRows : N;
+    f(h, r0, r1, seq_len_of(seq_lens, (int)(h / heads), N));
+  }
+}
+
+// Rows of a [heads_total, N, D] fp32 accumulator that lie inside their
+// sequence -> 0.
+template <int D>
+__device__ __forceinline__ void zero_real_rows(float* acc_f, long long heads_total,
+                                               int heads, int N,
+                                               const int* seq_lens) {
+  constexpr int kPerRow = D / 4;  // float4 per row
+  float4* acc = reinterpret_cast<float4*>(acc_f);
+  over_row_chunks(heads_total, heads, N, seq_lens,
+                  [&](long long h, int r0, int r1, int len) {
+    const int e = r1 < len ? r1 : len;
+    if (e <= r0) return;
+    float4* base = acc + ((size_t)h * N + r0) * kPerRow;
+    const int n = (e - r0) * kPerRow;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      base[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  });
+}
+
 // D_i = dO_i . O_i and LSE2_i = -LSE_i log2(e) for every padded row (one warp
 // per row, four rows in flight per warp); then the dQ accumulator is cleared.
 template <int D>
@@ -686,6 +725,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       }
     }
   }
+  if (a.seq_lens) {
+    // With per-sequence lengths only the real rows are cleared: padding rows of the accumulators are never read (the post kernel
+    // writes zeros there), whatever reductions reach them.
+    zero_real_rows<D>(a.dq_acc, a.BH, a.H, a.N, a.seq_lens);
+    if (a.nsplit > 1) {
+      zero_real_rows<D>(a.dk_acc, a.BHkv, a.Hkv, a.N, a.seq_lens);
+      zero_real_rows<D>(a.dv_acc, a.BHkv, a.Hkv, a.N, a.seq_lens);
+    }
+    return;
+  }
   const long long n4 = (long long)a.BH * a.N * D / 4;
   float4* acc = reinterpret_cast<float4*>(a.dq_acc);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n4;
@@ -718,41 +767,56 @@ __device__ __forceinline__ void round_rows(const float* acc_f, __nv_bfloat16* ou
   }
 }
 
-// Rows at or past their sequence's end -> 0 in a [heads_total, N, d] bf16
-// tensor whose batch entry is head / heads (eight elements per step).
-__device__ __forceinline__ void zero_tail_rows(__nv_bfloat16* out_b,
-                                               long long heads_total, int heads,
-                                               int N, int d,
-                                               const int* seq_lens) {
+// Per-sequence lengths: out = mul * acc -> bf16 on the rows inside each
+// sequence and 0 on the rows past its end (acc not read there), for a
+// [heads_total, N, d] tensor; acc == nullptr: only the zeros are written.
+__device__ __forceinline__ void round_rows_varlen(const float* acc_f,
+                                                  __nv_bfloat16* out_b,
+                                                  long long heads_total,
+                                                  int heads, int N, int d,
+                                                  float mul,
+                                                  const int* seq_lens) {
+  const int per_row = d / 8;  // groups of eight elements
+  const float4* acc = reinterpret_cast<const float4*>(acc_f);
   uint4* out = reinterpret_cast<uint4*>(out_b);
-  const int per_row = d / 8;
-  const long long n8 = heads_total * N * per_row;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n8;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long row = idx / per_row;
-    const long long h = row / N;
-    const int q = (int)(row - h * N);
-    if (q >= seq_len_of(seq_lens, (int)(h / heads), N))
-      out[idx] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  over_row_chunks(heads_total, heads, N, seq_lens,
+                  [&](long long h, int r0, int r1, int len) {
+    const int e = r1 < len ? r1 : (len > r0 ? len : r0);  // real rows [r0, e)
+    const size_t base = ((size_t)h * N + r0) * per_row;
+    const int n_real = (e - r0) * per_row, n_all = (r1 - r0) * per_row;
+    if (acc) {
+      for (int i = threadIdx.x; i < n_real; i += blockDim.x) {
+        const float4 x = acc[2 * (base + i)], y = acc[2 * (base + i) + 1];
+        out[base + i] = make_uint4(pack_bf16(x.x * mul, x.y * mul),
+                                   pack_bf16(x.z * mul, x.w * mul),
+                                   pack_bf16(y.x * mul, y.y * mul),
+                                   pack_bf16(y.z * mul, y.w * mul));
+      }
+    }
+    for (int i = n_real + threadIdx.x; i < n_all; i += blockDim.x)
+      out[base + i] = make_uint4(0u, 0u, 0u, 0u);
+  });
 }
 
 // dQ = scale * accumulator -> bf16, eight elements per thread per step; with
 // split key/value groups also dK and dV (already scaled) -> bf16.  With
-// per-sequence lengths the rows past each sequence's end of dQ, dK and dV
-// are then set to zero (the same thread rewrites the same elements, so the
-// zeros land last).
+// per-sequence lengths the same row by row, padding rows of dQ, dK and dV
+// set to zero without reading the accumulators there.
 __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
+  if (a.seq_lens) {
+    const bool split = a.nsplit > 1;
+    round_rows_varlen(a.dq_acc, a.dq, a.BH, a.H, a.N, d, a.scale, a.seq_lens);
+    round_rows_varlen(split ? a.dk_acc : nullptr, a.dk, a.BHkv, a.Hkv, a.N, d,
+                      1.0f, a.seq_lens);
+    round_rows_varlen(split ? a.dv_acc : nullptr, a.dv, a.BHkv, a.Hkv, a.N, d,
+                      1.0f, a.seq_lens);
+    return;
+  }
   round_rows(a.dq_acc, a.dq, (long long)a.BH * a.N * d / 8, a.scale);
   if (a.nsplit > 1) {
     const long long m8 = (long long)a.BHkv * a.N * d / 8;
     round_rows(a.dk_acc, a.dk, m8, 1.0f);
     round_rows(a.dv_acc, a.dv, m8, 1.0f);
-  }
-  if (a.seq_lens) {
-    zero_tail_rows(a.dq, a.BH, a.H, a.N, d, a.seq_lens);
-    zero_tail_rows(a.dk, a.BHkv, a.Hkv, a.N, d, a.seq_lens);
-    zero_tail_rows(a.dv, a.BHkv, a.Hkv, a.N, d, a.seq_lens);
   }
 }
 
