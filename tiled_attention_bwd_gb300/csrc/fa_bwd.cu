@@ -673,7 +673,10 @@ __device__ __forceinline__ void zero_real_rows(float* acc_f, long long heads_tot
 }
 
 // D_i = dO_i . O_i and LSE2_i = -LSE_i log2(e) for every padded row (one warp
-// per row, four rows in flight per warp); then the dQ accumulator is cleared.
+// per row, four rows in flight per warp), clearing the dQ accumulator of each
+// real row in the same pass (with per-sequence lengths, padding rows are
+// never read: the post kernel writes zeros there); then the split groups'
+// dK and dV accumulators.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   constexpr int kRows = 4;
@@ -707,6 +710,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
           ov[k][0] = *reinterpret_cast<const uint32_t*>(a.o + base);
           dv[k][0] = *reinterpret_cast<const uint32_t*>(a.dout + base);
         }
+        // The row's dQ accumulator is cleared in the same pass, so that the
+        // writes overlap the reads instead of following them.
+        float4* acc = reinterpret_cast<float4*>(a.dq_acc) + (size_t)lrow[k] * (D / 4);
+        for (int c = lane; c < D / 4; c += 32) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
@@ -725,22 +732,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       }
     }
   }
-  if (a.seq_lens) {
-    // With per-sequence lengths only the real rows are cleared: padding rows of the accumulators are never read (the post kernel
-    // writes zeros there), whatever reductions reach them.
-    zero_real_rows<D>(a.dq_acc, a.BH, a.H, a.N, a.seq_lens);
-    if (a.nsplit > 1) {
+  if (a.nsplit > 1) {
+    if (a.seq_lens) {
+      // With per-sequence lengths only real rows are cleared: the post
+      // kernel writes zeros on padding rows without reading them.
       zero_real_rows<D>(a.dk_acc, a.BHkv, a.Hkv, a.N, a.seq_lens);
       zero_real_rows<D>(a.dv_acc, a.BHkv, a.Hkv, a.N, a.seq_lens);
+      return;
     }
-    return;
-  }
-  const long long n4 = (long long)a.BH * a.N * D / 4;
-  float4* acc = reinterpret_cast<float4*>(a.dq_acc);
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n4;
-       idx += (long long)gridDim.x * blockDim.x)
-    acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.nsplit > 1) {
     const long long m4 = (long long)a.BHkv * a.N * D / 4;
     float4* ak = reinterpret_cast<float4*>(a.dk_acc);
     float4* av = reinterpret_cast<float4*>(a.dv_acc);
