@@ -136,6 +136,20 @@ def _check_qkv(name, t, shape=None):
             name, tuple(t.shape), tuple(shape)))
 
 
+def _check_lse(lse, B, H, N):
+    if not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 \
+            or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+
+
+def _lse_buffer(lse, B, H, N, device):
+    """A forward's LSE output: the caller's tensor (checked) or a new one."""
+    if lse is None:
+        return torch.empty((B, H, N), dtype=torch.float32, device=device)
+    _check_lse(lse, B, H, N)
+    return lse
+
+
 def fa_status_string(status: int) -> str:
     return load_library().fa_status_string(int(status)).decode()
 
@@ -181,11 +195,7 @@ def fa_fwd(q, k, v, causal: bool, scale: float, out=None, lse=None):
     if out is None:
         out = torch.empty_like(q)
     _check_qkv("out", out, q.shape)
-    if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    lse = _lse_buffer(lse, B, H, N, q.device)
     with torch.cuda.device(q.device):
         _check("fa_fwd", lib.fa_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
@@ -200,9 +210,7 @@ def fa_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None,
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_qkv(name, t, q.shape)
     B, H, N, d = q.shape
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    _check_lse(lse, B, H, N)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -241,12 +249,9 @@ def _check_ext_shapes(q, k):
     return B, H, Hkv, N, d
 
 
-def fa_fwd_ext(q, k, v, causal: bool, scale: float, window: int = -1,
-               out=None, lse=None):
-    """Forward pass with Hkv = k.shape[1] key/value heads shared by the
-    query heads (grouped / multi-query attention) and an optional sliding
-    window (|i - j| <= window; < 0: none).  Returns (O, LSE)."""
-    lib = load_library()
+def _ext_forward_buffers(q, k, v, out, lse):
+    """Checks of the grouped-head forward's tensors; returns the sizes and
+    the output buffers (allocated when not given)."""
     B, H, Hkv, N, d = _check_ext_shapes(q, k)
     _check_qkv("q", q)
     _check_qkv("k", k, (B, Hkv, N, d))
@@ -254,14 +259,42 @@ def fa_fwd_ext(q, k, v, causal: bool, scale: float, window: int = -1,
     if out is None:
         out = torch.empty_like(q)
     _check_qkv("out", out, q.shape)
-    if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    return (B, H, Hkv, N, d), out, _lse_buffer(lse, B, H, N, q.device)
+
+
+def _ext_backward_buffers(q, k, v, o, lse, dout, dq, dk, dv, workspace):
+    """Checks of the grouped-head backward's tensors; returns the sizes, the
+    gradient buffers and the workspace (allocated when not given)."""
+    B, H, Hkv, N, d = _check_ext_shapes(q, k)
+    _check_qkv("q", q)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    for name, t in (("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    _check_lse(lse, B, H, N)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_qkv("dq", dq, q.shape)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, Hkv, N, d))
+    if workspace is None:
+        need = fa_bwd_ext_workspace_size(B, H, Hkv, N, d)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=q.device)
+    return (B, H, Hkv, N, d), (dq, dk, dv), workspace
+
+
+def fa_fwd_ext(q, k, v, causal: bool, scale: float, window: int = -1,
+               out=None, lse=None):
+    """Forward pass with Hkv = k.shape[1] key/value heads shared by the
+    query heads (grouped / multi-query attention) and an optional sliding
+    window (|i - j| <= window; < 0: none).  Returns (O, LSE)."""
+    lib = load_library()
+    dims, out, lse = _ext_forward_buffers(q, k, v, out, lse)
     with torch.cuda.device(q.device):
         _check("fa_fwd_ext", lib.fa_fwd_ext(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), *dims,
             int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))
     return out, lse
@@ -272,30 +305,13 @@ def fa_bwd_ext(q, k, v, o, lse, dout, causal: bool, scale: float,
     """Backward of fa_fwd_ext.  Returns (dQ [B,H,N,d], dK, dV [B,Hkv,N,d]);
     dK and dV are summed over the query heads sharing each K/V head."""
     lib = load_library()
-    B, H, Hkv, N, d = _check_ext_shapes(q, k)
-    _check_qkv("q", q)
-    for name, t in (("k", k), ("v", v)):
-        _check_qkv(name, t, (B, Hkv, N, d))
-    for name, t in (("o", o), ("dout", dout)):
-        _check_qkv(name, t, q.shape)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    _check_qkv("dq", dq, q.shape)
-    for name, t in (("dk", dk), ("dv", dv)):
-        _check_qkv(name, t, (B, Hkv, N, d))
-    need = fa_bwd_ext_workspace_size(B, H, Hkv, N, d)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
-                                device=q.device)
+    dims, (dq, dk, dv), workspace = _ext_backward_buffers(
+        q, k, v, o, lse, dout, dq, dk, dv, workspace)
     with torch.cuda.device(q.device):
         _check("fa_bwd_ext", lib.fa_bwd_ext(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+            workspace.numel() * workspace.element_size(), *dims,
             int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))
     return dq, dk, dv
@@ -318,23 +334,12 @@ def fa_fwd_varlen(q, k, v, seq_lens, causal: bool, scale: float,
     [0, N]).  Rows past a sequence's end of the returned O and LSE are left
     as they were (unwritten).  Returns (O, LSE)."""
     lib = load_library()
-    B, H, Hkv, N, d = _check_ext_shapes(q, k)
-    _check_qkv("q", q)
-    _check_qkv("k", k, (B, Hkv, N, d))
-    _check_qkv("v", v, (B, Hkv, N, d))
-    _check_seq_lens(seq_lens, B, q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    _check_qkv("out", out, q.shape)
-    if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    dims, out, lse = _ext_forward_buffers(q, k, v, out, lse)
+    _check_seq_lens(seq_lens, dims[0], q.device)
     with torch.cuda.device(q.device):
         _check("fa_fwd_varlen", lib.fa_fwd_varlen(
             _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seq_lens),
-            B, H, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+            *dims, int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))
     return out, lse
 
@@ -345,31 +350,14 @@ def fa_bwd_varlen(q, k, v, o, lse, dout, seq_lens, causal: bool,
     """Backward of fa_fwd_varlen.  Returns (dQ [B,H,N,d], dK, dV [B,Hkv,N,d])
     with every row past its sequence's end set to zero."""
     lib = load_library()
-    B, H, Hkv, N, d = _check_ext_shapes(q, k)
-    _check_qkv("q", q)
-    for name, t in (("k", k), ("v", v)):
-        _check_qkv(name, t, (B, Hkv, N, d))
-    for name, t in (("o", o), ("dout", dout)):
-        _check_qkv(name, t, q.shape)
-    _check_seq_lens(seq_lens, B, q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    _check_qkv("dq", dq, q.shape)
-    for name, t in (("dk", dk), ("dv", dv)):
-        _check_qkv(name, t, (B, Hkv, N, d))
-    need = fa_bwd_ext_workspace_size(B, H, Hkv, N, d)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
-                                device=q.device)
+    dims, (dq, dk, dv), workspace = _ext_backward_buffers(
+        q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    _check_seq_lens(seq_lens, dims[0], q.device)
     with torch.cuda.device(q.device):
         _check("fa_bwd_varlen", lib.fa_bwd_varlen(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(seq_lens), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+            workspace.numel() * workspace.element_size(), *dims,
             int(bool(causal)), int(window), float(scale),
             _stream_handle(q.device)))
     return dq, dk, dv
@@ -391,11 +379,7 @@ def fa_fwd_fp8(q, k, v, causal: bool, scale: float, out=None, lse=None,
     if out is None:
         out = torch.empty_like(q)
     _check_qkv("out", out, q.shape)
-    if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    lse = _lse_buffer(lse, B, H, N, q.device)
     if workspace is None:
         need = fa_fwd_fp8_workspace_size(B, H, N, d)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8,
@@ -481,9 +465,7 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, causal: bool, scale: float, dq,
                     ("dq", dq), ("dk", dk), ("dv", dv)):
         _check_qkv(name, t, q.shape)
     B, H, N, d = q.shape
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
-            or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B,H,N]")
+    _check_lse(lse, B, H, N)
     with torch.cuda.device(q.device):
         _check("fa_bwd_noalloc", lib.fa_bwd_noalloc(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
