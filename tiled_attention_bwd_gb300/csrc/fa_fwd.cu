@@ -183,7 +183,7 @@ struct FwdItem {
 // list of non-empty items in decreasing cost:
 //   np[b]    pairs of Q tiles of sequence b (ceil(tiles / 2));
 //   order[s] sequences by decreasing np (ties by index: every block gets the
-//            same order, so the item lists agree);
+//            same order, so the item lists agree), by a counting sort;
 //   pref[x]  item counts before group x, where a group is a pair index from
 //            the last one down (causal: a pair's cost is the same for every
 //            sequence that has it, and the sequences that have pair p are the
@@ -193,26 +193,58 @@ struct FwdItem {
 template <bool CAUSAL>
 __device__ int build_item_table(int* tab, const FwdArgs& a, int n_pairs) {
   const int B = a.BH / a.H;
+  const int X = CAUSAL ? n_pairs : B;
   int* np = tab;
   int* order = tab + B;
   int* pref = tab + 2 * B;
+  int* start = pref + X + 1;  // [n_pairs + 1]: counting-sort bins
   const int tid = threadIdx.x, nt = blockDim.x;
+  for (int v = tid; v <= n_pairs; v += nt) start[v] = 0;
   for (int b = tid; b < B; b += nt) {
     const int tiles = (seq_len_of(a.seq_lens, b, a.N) + kTile - 1) / kTile;
-    np[b] = (tiles + 1) / 2;
+    np[b] = (tiles + 1) / 2;  // <= n_pairs: lengths are clamped to N
   }
   __syncthreads();
-  for (int b = tid; b < B; b += nt) {
-    const int v = np[b];
-    int rank = 0;
-    for (int b2 = 0; b2 < B; ++b2) {
-      const int v2 = np[b2];
-      rank += (v2 > v) || (v2 == v && b2 < b);
+  for (int b = tid; b < B; b += nt) atomicAdd(&start[np[b]], 1);
+  __syncthreads();
+  // Stable counting sort by decreasing np, by one warp: start[v] becomes the
+  // number of sequences with more pairs than v, then 32 sequences are placed
+  // per step in index order (equal values ranked by lane), so every block
+  // builds the same order.
+  if (tid < 32) {
+    const int V = n_pairs + 1;  // bins, taken from the largest value down
+    const int chunk = (V + 31) / 32;
+    const int r0 = tid * chunk, r1 = min(V, r0 + chunk);
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) sum += start[n_pairs - r];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += t;
     }
-    order[rank] = b;
+    int run = incl - sum;
+    for (int r = r0; r < r1; ++r) {
+      const int c = start[n_pairs - r];
+      start[n_pairs - r] = run;
+      run += c;
+    }
+    __syncwarp();
+    for (int c0 = 0; c0 < B; c0 += 32) {
+      const int b = c0 + tid;
+      const int v = b < B ? np[b] : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, v);
+      const int rank = __popc(grp & ((1u << tid) - 1u));
+      const int base = b < B ? start[v] : 0;
+      __syncwarp();
+      if (b < B) {
+        order[base + rank] = b;
+        if (rank == 0) start[v] = base + __popc(grp);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
-  const int X = CAUSAL ? n_pairs : B;
   for (int x = tid; x < X; x += nt) {
     int cnt;
     if (CAUSAL) {  // sequences with more than p pairs: a prefix of `order`
@@ -787,11 +819,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   size_t smem_bytes = L::kSmemBytes;
   args.sched = 0;
   if constexpr (VARLEN) {
-    // The balanced item table (np, order: B ints each; pref: groups + 1)
-    // when it fits in the shared memory left by the tiles.
+    // The balanced item table (np, order: B ints each; pref: groups + 1;
+    // sort bins: pairs + 1) when it fits in the shared memory left by the
+    // tiles.
     const long long B = a.BH / a.H;
     const long long groups = CAUSAL ? n_pairs : B;
-    const long long table = 4 * (2 * B + groups + 1);
+    const long long table = 4 * (2 * B + groups + 1 + n_pairs + 1);
     int dev = 0, optin = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
