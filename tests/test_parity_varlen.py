@@ -120,6 +120,23 @@ def test_varlen_every_element(B, H, Hkv, N, d, causal, window, fixed):
     check_grads(got, lens, inp, causal, scale, window, tag)
 
 
+@pytest.mark.parametrize("lens,causal", [([0, 0, 0], True),
+                                         ([260, -3, 7], False),
+                                         ([999, 0, 300], True)])
+def test_empty_and_out_of_range_lengths(lens, causal):
+    # Every sequence empty: nothing is written but zero gradients.  Lengths
+    # outside [0, N] are clamped (N = 300 here).
+    B, H, Hkv, N, d = 3, 2, 1, 300, 64
+    inp = make_grouped_inputs(B, H, Hkv, N, d, seed=55)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    scale = default_scale(d)
+    tag = "lens=%s causal=%d" % (lens.tolist(), causal)
+    got = run_varlen(inp, lens, causal, scale, -1)
+    clamped = lens.clamp(0, N)
+    check_rows(got, clamped, inp, causal, scale, -1, tag)
+    check_grads(got, clamped, inp, causal, scale, -1, tag)
+
+
 @pytest.mark.parametrize("B,causal", [(2000, False), (4400, True),
                                       (4400, False)])
 def test_many_short_sequences(B, causal):
