@@ -31,8 +31,9 @@
  *  - scale multiplies Q K^T before the mask and the softmax; it must be finite
  *    and > 0 (usually 1/sqrt(d)).
  *  - Supported: d in {64, 128}; 1 <= N <= 2^30 of any size (tiles past N
- *    are masked); B, H >= 1 with B*H <= INT_MAX.  B, H or N equal to 0 is an empty problem: the call returns
- *    FA_OK and touches nothing (pointers may then be NULL).
+ *    are masked); B, H >= 1 with B*H <= INT_MAX.  B, H or N equal to 0 is
+ *    an empty problem: the call returns FA_OK and touches nothing (pointers
+ *    may then be NULL).
  *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Every compute entry point is asynchronous on that stream:
  *    FA_OK means the kernels were launched.  A failure detected on the device
