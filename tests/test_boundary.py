@@ -268,3 +268,45 @@ def test_fp8_workspace_size(lib, B, H, N, d):
     expect = 2 * _align(B * H * N * d) + 2 * _align(B * H * nsb * 4)
     assert lib.fa_fwd_fp8_workspace_size(B, H, N, d) == expect
     assert lib.fa_fwd_fp8_workspace_size(B, H, N, 64) == 0
+
+
+def _step_host(lib, ptr=256, scratch=256, scratch_bytes=1 << 40, B=2, H=8,
+               N=512, d=128, causal=1, scale=0.125, chunk=0):
+    p = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.fa_step_host(p(ptr), p(ptr), p(ptr), p(ptr), p(ptr), p(ptr),
+                            p(ptr), p(ptr), p(ptr), p(scratch), scratch_bytes,
+                            B, H, N, d, causal, scale, chunk, None)
+
+
+@pytest.mark.parametrize("B,H,N,d,chunk", [(2, 8, 512, 128, 0),
+                                          (2, 8, 512, 128, 5),
+                                          (1, 3, 333, 64, 1),
+                                          (1, 4, 256, 128, 100),
+                                          (4, 64, 4096, 128, 0)])
+def test_step_host_scratch_size(lib, B, H, N, d, chunk):
+    # Three rotating slots; each holds eight [ch,N,d] bf16 tensors, the LSE
+    # rows and the backward workspace of ch heads, each 256-byte aligned.
+    BH = B * H
+    ch = min(chunk, BH) if chunk > 0 else (BH + 15) // 16
+    slot = (8 * _align(ch * N * d * 2) + _align(ch * N * 4)
+            + _align(lib.fa_bwd_workspace_size(1, ch, N, d)))
+    assert lib.fa_step_host_scratch_size(B, H, N, d, chunk) == 3 * slot
+    assert lib.fa_step_host_scratch_size(0, H, N, d, chunk) == 0
+    assert lib.fa_step_host_scratch_size(B, H, N, 96, chunk) == 0
+
+
+def test_step_host_argument_checks(lib):
+    assert _step_host(lib, chunk=-1) == INVALID
+    assert _step_host(lib, ptr=0) == INVALID
+    assert _step_host(lib, scale=0.0) == INVALID
+    assert _step_host(lib, d=96) == UNSUPPORTED
+    assert _step_host(lib, scratch=0) == WORKSPACE
+    assert _step_host(lib, scratch=128) == WORKSPACE      # not 256-aligned
+    need = lib.fa_step_host_scratch_size(2, 8, 512, 128, 0)
+    assert _step_host(lib, scratch_bytes=need - 1) == WORKSPACE
+    assert _step_host(lib, ptr=0, scratch=0, N=0) == OK   # empty problem
+
+
+def test_phase_events_can_be_cleared(lib):
+    # Null events turn the recording off; nothing is launched.
+    lib.fa_bwd_set_phase_events(None, None)
