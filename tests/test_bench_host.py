@@ -125,3 +125,28 @@ def test_step_flops_with_sequence_lengths():
     assert drawn.dtype.is_floating_point is False and len(drawn) == w.B
     assert all(1 <= int(x) <= w.N for x in drawn)
     assert bench.bench_lengths(w).tolist() == drawn.tolist()    # seeded
+
+
+def test_reference_arm_records_the_lengths():
+    import subprocess
+    import sys
+    out = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+         "reference", "--steps", "1", "--warmup", "0", "--workload",
+         "small_2x8x512x64", "--varlen"],
+        capture_output=True, text=True, timeout=300, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    from tiled_attention_bwd_gb300.workloads import WORKLOADS
+    w = WORKLOADS["small_2x8x512x64"]
+    assert line["config"]["seq_lens"] == bench.bench_lengths(w).tolist()
+
+
+def test_varlen_and_fp8_are_exclusive():
+    import subprocess
+    import sys
+    r = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--varlen", "--fp8",
+         "--steps", "1", "--warmup", "3"],
+        capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "--varlen" in (r.stderr + r.stdout)
