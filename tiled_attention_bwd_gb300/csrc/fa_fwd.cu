@@ -59,12 +59,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_t (bf16 pairs) is written over the first 64 columns of S_t.
 //
-// Measured on this part: a lone chain of M=128 tcgen05 MMAs with both
-// operands in smem runs at about 40% of peak, one with A in TMEM at full
-// rate, and the forward's interleaving of S = Q K^T (smem x smem) with
-// O += P V (TMEM x smem) runs at full rate; MMAs with N or K of 64 run well
-// below it.  Hence 128-key tiles, P kept in TMEM, and two Q tiles whose MMAs
-// interleave.
+// Measured on this part: in a chain of M=128 tcgen05 MMAs as an earlier
+// probe issued them, both operands in smem ran at about 40% of peak and A in
+// TMEM at full rate; MMAs with N or K of 64 ran well below it; and the
+// forward's interleaving of S = Q K^T (smem x smem) with O += P V (TMEM x
+// smem) ran at full rate.  Issued back to back with no waits, every form runs
+// at full rate, so the smem x smem cost is latency on a dependent path.
+// Hence 128-key tiles, P kept in TMEM, and two Q tiles whose MMAs interleave.
 template <int D>
 struct FwdLayout {
   static constexpr int kSub = D / 64;             // 64-column sub-tiles
