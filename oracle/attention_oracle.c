@@ -104,32 +104,34 @@ static double row_scores_lse(const double* qi, const double* k, int64_t nvis,
  * Forward.  q, k, v, o: [BH, N, d] row-major doubles; lse: [BH, N].
  * P_ij = exp(s_ij - lse_i); O_i = sum_j P_ij v_j.
  * The _rows variant computes only query rows r0 <= i < r1 (each row is
- * independent) and leaves the other rows of o and lse untouched.
+ * independent) and leaves the other rows of o and lse untouched.  Every
+ * (head, row) is independent of every other, so they are spread over the
+ * OpenMP threads one by one; each row's arithmetic is the same whichever
+ * thread runs it.
  */
 void oracle_fwd_rows(const double* q, const double* k, const double* v,
                      int64_t BH, int64_t N, int64_t d, int causal,
                      double scale, int64_t r0, int64_t r1, double* o,
                      double* lse) {
+  const int64_t rows = r1 > r0 ? r1 - r0 : 0;
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t bh = 0; bh < BH; ++bh) {
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < BH * rows; ++u) {
+      const int64_t bh = u / rows, i = r0 + u % rows;
       const double* qh = q + bh * N * d;
       const double* kh = k + bh * N * d;
       const double* vh = v + bh * N * d;
-      double* oh = o + bh * N * d;
-      for (int64_t i = r0; i < r1; ++i) {
-        int64_t nvis = visible_keys(i, N, causal);
-        double l = row_scores_lse(qh + i * d, kh, nvis, d, scale, s);
-        lse[bh * N + i] = l;
-        double* oi = oh + i * d;
-        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) {
-          double p = exp(s[j] - l);
-          const double* vj = vh + j * d;
-          for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
-        }
+      int64_t nvis = visible_keys(i, N, causal);
+      double l = row_scores_lse(qh + i * d, kh, nvis, d, scale, s);
+      lse[bh * N + i] = l;
+      double* oi = o + (bh * N + i) * d;
+      for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int64_t j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - l);
+        const double* vj = vh + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
       }
     }
     free(s);
@@ -205,10 +207,20 @@ void oracle_fwd_online(const double* q, const double* k, const double* v,
 
 /*
  * Backward.  q, k, v, dout: [BH, N, d]; outputs dq, dk, dv: [BH, N, d].
- * Per query row i: recompute the scores and lse_i, P_ij = exp(s_ij - lse_i),
- * O_i = sum_j P_ij v_j, D_i = dO_i . O_i; then for each visible key j:
+ * Per query row i: the scores and lse_i, P_ij = exp(s_ij - lse_i),
+ * O_i = sum_j P_ij v_j and D_i = dO_i . O_i; then, for each visible pair
+ * (i, j):
  *   dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
  *   dQ_i += scale dS_ij k_j,  dK_j += scale dS_ij q_i,  dV_j += P_ij dO_i.
+ * The sums are taken in two passes so that rows and keys can be spread over
+ * threads with no two threads adding into the same output row:
+ *   pass 1, one query row at a time: lse_i, O_i, D_i and dQ_i (sum over j
+ *           in increasing order);
+ *   pass 2, one key at a time: dK_j and dV_j, summing over the rows i that
+ *           see key j in increasing order, with P_ij and dS_ij recomputed
+ *           from the same expressions and the saved lse_i, D_i.
+ * Each output element is the same sum, in the same order, as one loop over
+ * i (outer) and j (inner) would take.
  * The _rows variant sums the contributions of query rows r0 <= i < r1 only:
  * dq is exact on those rows (zero elsewhere); dk and dv hold the partial sums
  * over those rows, which are the full gradients for keys j >= r0 when causal
@@ -218,54 +230,67 @@ void oracle_bwd_rows(const double* q, const double* k, const double* v,
                      const double* dout, int64_t BH, int64_t N, int64_t d,
                      int causal, double scale, int64_t r0, int64_t r1,
                      double* dq, double* dk, double* dv) {
+  const int64_t rows = r1 > r0 ? r1 - r0 : 0;
+  double* lse_s = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+  double* dd_s = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+  memset(dq, 0, sizeof(double) * (size_t)(BH * N * d));
+  memset(dk, 0, sizeof(double) * (size_t)(BH * N * d));
+  memset(dv, 0, sizeof(double) * (size_t)(BH * N * d));
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double* oi = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t bh = 0; bh < BH; ++bh) {
-      const double* qh = q + bh * N * d;
+    /* pass 1: query rows */
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < BH * rows; ++u) {
+      const int64_t bh = u / rows, i = r0 + u % rows;
       const double* kh = k + bh * N * d;
       const double* vh = v + bh * N * d;
-      const double* doh = dout + bh * N * d;
-      double* dqh = dq + bh * N * d;
-      double* dkh = dk + bh * N * d;
-      double* dvh = dv + bh * N * d;
-      memset(dqh, 0, sizeof(double) * (size_t)(N * d));
-      memset(dkh, 0, sizeof(double) * (size_t)(N * d));
-      memset(dvh, 0, sizeof(double) * (size_t)(N * d));
+      int64_t nvis = visible_keys(i, N, causal);
+      const double* qi = q + (bh * N + i) * d;
+      const double* doi = dout + (bh * N + i) * d;
+      double l = row_scores_lse(qi, kh, nvis, d, scale, s);
+      for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int64_t j = 0; j < nvis; ++j) {
+        s[j] = exp(s[j] - l); /* s now holds P_ij */
+        const double* vj = vh + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += s[j] * vj[t];
+      }
+      double D = dot(doi, oi, d);
+      lse_s[bh * N + i] = l;
+      dd_s[bh * N + i] = D;
+      double* dqi = dq + (bh * N + i) * d;
+      for (int64_t j = 0; j < nvis; ++j) {
+        double ds = s[j] * (dot(doi, vh + j * d, d) - D);
+        const double* kj = kh + j * d;
+        for (int64_t t = 0; t < d; ++t) dqi[t] += scale * ds * kj[t];
+      }
+    }
+    /* pass 2: keys (the implicit barrier above orders it after pass 1) */
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < BH * N; ++u) {
+      const int64_t bh = u / N, j = u % N;
+      const double* kj = k + (bh * N + j) * d;
+      const double* vj = v + (bh * N + j) * d;
+      double* dkj = dk + (bh * N + j) * d;
+      double* dvj = dv + (bh * N + j) * d;
       for (int64_t i = r0; i < r1; ++i) {
-        int64_t nvis = visible_keys(i, N, causal);
-        const double* qi = qh + i * d;
-        const double* doi = doh + i * d;
-        double l = row_scores_lse(qi, kh, nvis, d, scale, s);
-        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) {
-          s[j] = exp(s[j] - l); /* s now holds P_ij */
-          const double* vj = vh + j * d;
-          for (int64_t t = 0; t < d; ++t) oi[t] += s[j] * vj[t];
-        }
-        double D = dot(doi, oi, d);
-        double* dqi = dqh + i * d;
-        for (int64_t j = 0; j < nvis; ++j) {
-          double p = s[j];
-          const double* kj = kh + j * d;
-          const double* vj = vh + j * d;
-          double dp = dot(doi, vj, d);
-          double ds = p * (dp - D);
-          double* dkj = dkh + j * d;
-          double* dvj = dvh + j * d;
-          for (int64_t t = 0; t < d; ++t) {
-            dqi[t] += scale * ds * kj[t];
-            dkj[t] += scale * ds * qi[t];
-            dvj[t] += p * doi[t];
-          }
+        if (j >= visible_keys(i, N, causal)) continue;
+        const double* qi = q + (bh * N + i) * d;
+        const double* doi = dout + (bh * N + i) * d;
+        double p = exp(scale * dot(qi, kj, d) - lse_s[bh * N + i]);
+        double ds = p * (dot(doi, vj, d) - dd_s[bh * N + i]);
+        for (int64_t t = 0; t < d; ++t) {
+          dkj[t] += scale * ds * qi[t];
+          dvj[t] += p * doi[t];
         }
       }
     }
     free(oi);
     free(s);
   }
+  free(dd_s);
+  free(lse_s);
 }
 
 void oracle_bwd(const double* q, const double* k, const double* v,
@@ -278,36 +303,36 @@ void oracle_bwd(const double* q, const double* k, const double* v,
  * Grouped / multi-query attention with an optional sliding window.
  * q, o: [B, H, N, d]; k, v: [B, Hkv, N, d] with H % Hkv == 0; query head h
  * reads key/value head h / (H / Hkv).  Visible keys as in visible_range.
- * Rows r0 <= i < r1 only (the other rows of o and lse are untouched).
+ * Rows r0 <= i < r1 only (the other rows of o and lse are untouched); every
+ * (query head, row) is independent and they are spread over the threads.
  */
 void oracle_fwd_ext_rows(const double* q, const double* k, const double* v,
                          int64_t B, int64_t H, int64_t Hkv, int64_t N,
                          int64_t d, int causal, int64_t window, double scale,
                          int64_t r0, int64_t r1, double* o, double* lse) {
   const int64_t group = H / Hkv;
+  const int64_t rows = r1 > r0 ? r1 - r0 : 0;
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t bh = 0; bh < B * H; ++bh) {
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < B * H * rows; ++u) {
+      const int64_t bh = u / rows, i = r0 + u % rows;
       const int64_t b = bh / H, h = bh % H;
       const int64_t bkv = b * Hkv + h / group;
-      const double* qh = q + bh * N * d;
       const double* kh = k + bkv * N * d;
       const double* vh = v + bkv * N * d;
-      double* oh = o + bh * N * d;
-      for (int64_t i = r0; i < r1; ++i) {
-        int64_t lo, hi;
-        visible_range(i, N, causal, window, &lo, &hi);
-        const double l = row_scores_lse_range(qh + i * d, kh, lo, hi, d, scale, s);
-        lse[bh * N + i] = l;
-        double* oi = oh + i * d;
-        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
-        for (int64_t j = lo; j < hi; ++j) {
-          const double p = exp(s[j - lo] - l);
-          const double* vj = vh + j * d;
-          for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
-        }
+      int64_t lo, hi;
+      visible_range(i, N, causal, window, &lo, &hi);
+      const double l = row_scores_lse_range(q + (bh * N + i) * d, kh, lo, hi,
+                                            d, scale, s);
+      lse[bh * N + i] = l;
+      double* oi = o + (bh * N + i) * d;
+      for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int64_t j = lo; j < hi; ++j) {
+        const double p = exp(s[j - lo] - l);
+        const double* vj = vh + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += p * vj[t];
       }
     }
     free(s);
@@ -318,8 +343,10 @@ void oracle_fwd_ext_rows(const double* q, const double* k, const double* v,
  * Backward of the grouped / windowed forward: dq [B, H, N, d] per query
  * head; dk, dv [B, Hkv, N, d] summed over the query heads of each group
  * (each head's contribution is the chain rule of its own softmax, as in
- * oracle_bwd).  Query rows r0 <= i < r1 only contribute.  Work is split by
- * key/value head so that no two threads add into the same dk/dv rows.
+ * oracle_bwd_rows).  Query rows r0 <= i < r1 only contribute.  The same two
+ * passes as oracle_bwd_rows: query rows (lse_i, O_i, D_i, dQ_i), then keys
+ * (dK_j, dV_j summed over the group's query heads in order, and within a
+ * head over the rows that see key j in increasing order).
  */
 void oracle_bwd_ext_rows(const double* q, const double* k, const double* v,
                          const double* dout, int64_t B, int64_t H, int64_t Hkv,
@@ -327,51 +354,68 @@ void oracle_bwd_ext_rows(const double* q, const double* k, const double* v,
                          double scale, int64_t r0, int64_t r1, double* dq,
                          double* dk, double* dv) {
   const int64_t group = H / Hkv;
+  const int64_t rows = r1 > r0 ? r1 - r0 : 0;
+  const int64_t nrow = B * H * N;
+  double* lse_s = (double*)malloc(sizeof(double) * (size_t)(nrow > 0 ? nrow : 1));
+  double* dd_s = (double*)malloc(sizeof(double) * (size_t)(nrow > 0 ? nrow : 1));
   memset(dq, 0, sizeof(double) * (size_t)(B * H * N * d));
+  memset(dk, 0, sizeof(double) * (size_t)(B * Hkv * N * d));
+  memset(dv, 0, sizeof(double) * (size_t)(B * Hkv * N * d));
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double* oi = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t bkv = 0; bkv < B * Hkv; ++bkv) {
-      const int64_t b = bkv / Hkv, g = bkv % Hkv;
+    /* pass 1: query rows */
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < B * H * rows; ++u) {
+      const int64_t bh = u / rows, i = r0 + u % rows;
+      const int64_t b = bh / H, h = bh % H;
+      const int64_t bkv = b * Hkv + h / group;
       const double* kh = k + bkv * N * d;
       const double* vh = v + bkv * N * d;
-      double* dkh = dk + bkv * N * d;
-      double* dvh = dv + bkv * N * d;
-      memset(dkh, 0, sizeof(double) * (size_t)(N * d));
-      memset(dvh, 0, sizeof(double) * (size_t)(N * d));
+      const double* qi = q + (bh * N + i) * d;
+      const double* doi = dout + (bh * N + i) * d;
+      int64_t lo, hi;
+      visible_range(i, N, causal, window, &lo, &hi);
+      const double l = row_scores_lse_range(qi, kh, lo, hi, d, scale, s);
+      for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int64_t j = lo; j < hi; ++j) {
+        s[j - lo] = exp(s[j - lo] - l); /* now P_ij */
+        const double* vj = vh + j * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] += s[j - lo] * vj[t];
+      }
+      const double D = dot(doi, oi, d);
+      lse_s[bh * N + i] = l;
+      dd_s[bh * N + i] = D;
+      double* dqi = dq + (bh * N + i) * d;
+      for (int64_t j = lo; j < hi; ++j) {
+        const double ds = s[j - lo] * (dot(doi, vh + j * d, d) - D);
+        const double* kj = kh + j * d;
+        for (int64_t t = 0; t < d; ++t) dqi[t] += scale * ds * kj[t];
+      }
+    }
+    /* pass 2: keys of each key/value head */
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t u = 0; u < B * Hkv * N; ++u) {
+      const int64_t bkv = u / N, j = u % N;
+      const int64_t b = bkv / Hkv, g = bkv % Hkv;
+      const double* kj = k + (bkv * N + j) * d;
+      const double* vj = v + (bkv * N + j) * d;
+      double* dkj = dk + (bkv * N + j) * d;
+      double* dvj = dv + (bkv * N + j) * d;
       for (int64_t h = g * group; h < (g + 1) * group; ++h) {
         const int64_t bh = b * H + h;
-        const double* qh = q + bh * N * d;
-        const double* doh = dout + bh * N * d;
-        double* dqh = dq + bh * N * d;
         for (int64_t i = r0; i < r1; ++i) {
           int64_t lo, hi;
           visible_range(i, N, causal, window, &lo, &hi);
-          const double* qi = qh + i * d;
-          const double* doi = doh + i * d;
-          const double l = row_scores_lse_range(qi, kh, lo, hi, d, scale, s);
-          for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
-          for (int64_t j = lo; j < hi; ++j) {
-            s[j - lo] = exp(s[j - lo] - l); /* now P_ij */
-            const double* vj = vh + j * d;
-            for (int64_t t = 0; t < d; ++t) oi[t] += s[j - lo] * vj[t];
-          }
-          const double D = dot(doi, oi, d);
-          double* dqi = dqh + i * d;
-          for (int64_t j = lo; j < hi; ++j) {
-            const double p = s[j - lo];
-            const double* kj = kh + j * d;
-            const double* vj = vh + j * d;
-            const double ds = p * (dot(doi, vj, d) - D);
-            double* dkj = dkh + j * d;
-            double* dvj = dvh + j * d;
-            for (int64_t t = 0; t < d; ++t) {
-              dqi[t] += scale * ds * kj[t];
-              dkj[t] += scale * ds * qi[t];
-              dvj[t] += p * doi[t];
-            }
+          if (j < lo || j >= hi) continue;
+          const double* qi = q + (bh * N + i) * d;
+          const double* doi = dout + (bh * N + i) * d;
+          const double p = exp(scale * dot(qi, kj, d) - lse_s[bh * N + i]);
+          const double ds = p * (dot(doi, vj, d) - dd_s[bh * N + i]);
+          for (int64_t t = 0; t < d; ++t) {
+            dkj[t] += scale * ds * qi[t];
+            dvj[t] += p * doi[t];
           }
         }
       }
@@ -379,5 +423,6 @@ void oracle_bwd_ext_rows(const double* q, const double* k, const double* v,
     free(oi);
     free(s);
   }
+  free(dd_s);
+  free(lse_s);
 }
-
