@@ -5,11 +5,9 @@ limited to |i - j| <= window) against the CPU fp64 oracle's fwd_ext /
 bwd_ext on the same seeded bf16 inputs, with the tolerances of the base
 operation (O max-abs 2e-2 and rel-Frobenius 1e-2, LSE max-abs 1e-3, each
 gradient rel-Frobenius 5e-2).  Small shapes are compared element by element;
-full-size shapes on slices whose exact values the oracle computes from a row
-range (a key row's dK/dV is exact once every query row that sees it is in
-the range).  Identities: Hkv = H with no window is the base operation bit
-for bit; a window of N - 1 or more is no window; grouped heads equal
-repeated heads.
+full-size shapes on whole key/value groups, every row.  Identities: Hkv = H
+with no window is the base operation bit for bit; a window of N - 1 or more
+is no window; grouped heads equal repeated heads.
 """
 import numpy as np
 import pytest
@@ -181,61 +179,31 @@ FULL = [
 
 
 @pytest.mark.parametrize("name,B,H,Hkv,N,d,causal,window", FULL)
-def test_full_size_slices(name, B, H, Hkv, N, d, causal, window):
+def test_full_size_whole_groups(name, B, H, Hkv, N, d, causal, window):
     inp = make_grouped_inputs(B, H, Hkv, N, d, seed=2001 + H + Hkv + N)
     scale = default_scale(d)
     got = run_ext(inp, causal, scale, window)
     g = H // Hkv
-    # One key/value head (the last batch entry's last) with its query heads.
-    b, kvh = B - 1, Hkv - 1
-    hs = slice(kvh * g, (kvh + 1) * g)
-    sub = {"q": inp["q"][b:b + 1, hs], "do": inp["do"][b:b + 1, hs],
-           "k": inp["k"][b:b + 1, kvh:kvh + 1],
-           "v": inp["v"][b:b + 1, kvh:kvh + 1]}
-    # Query rows [r0, N): exact O, LSE, dQ there, and exact dK/dV for every
-    # key row k >= k0 whose visible queries all lie in [r0, N).
-    if causal or window < 0:
-        R = 256
-    else:
-        R = min(N, window + 256)
-    r0 = N - R
-    o_ref, lse_ref, dq, dk, dv = oracle_group_rows(sub, causal, scale, window,
-                                                   r0, N)
-    check_forward(got["o"][b:b + 1, hs, r0:], got["lse"][b:b + 1, hs, r0:],
-                  o_ref[:, :, r0:], lse_ref[:, :, r0:], name)
-    check_grad("dq", got["dq"][b:b + 1, hs, r0:], dq[:, :, r0:], name)
-    if causal:
-        k0 = r0                     # keys >= r0 are seen only by rows >= r0
-    elif window >= 0:
-        k0 = r0 + window            # key k is seen by rows >= k - w >= r0
-    else:
-        k0 = N
-    assert k0 < N or not causal
-    if k0 < N:
-        check_grad("dk", got["dk"][b:b + 1, kvh:kvh + 1, k0:], dk[:, :, k0:],
-                   name)
-        check_grad("dv", got["dv"][b:b + 1, kvh:kvh + 1, k0:], dv[:, :, k0:],
-                   name)
-    # First rows too (causal: they see few keys; window: the band's start).
-    o_ref, lse_ref = oracle.fwd_ext(sub["q"], sub["k"], sub["v"], causal,
-                                    scale, window, 0, 256)
-    check_forward(got["o"][b:b + 1, hs, :256], got["lse"][b:b + 1, hs, :256],
-                  o_ref[:, :, :256], lse_ref[:, :, :256], name + " head rows")
-
-
-def oracle_group_rows(sub, causal, scale, window, r0, r1):
-    """The oracle on one key/value head and its query heads, rows [r0, r1).
-    Each query head becomes a batch entry of its own with a copy of the K/V
-    head, so the oracle's threads split the heads; dK and dV of the group
-    are the sums over those entries, which is how the grouped operation
-    defines them."""
-    g = sub["q"].shape[1]
-    q = sub["q"].double().numpy().transpose(1, 0, 2, 3)      # [g,1,N,d]
-    do = sub["do"].double().numpy().transpose(1, 0, 2, 3)
-    k = np.repeat(sub["k"].double().numpy(), g, axis=0)      # [g,1,N,d]
-    v = np.repeat(sub["v"].double().numpy(), g, axis=0)
-    o, lse = oracle.fwd_ext(q, k, v, causal, scale, window, r0, r1)
-    dq, dk, dv = oracle.bwd_ext(q, k, v, do, causal, scale, window, r0, r1)
-    return (o.transpose(1, 0, 2, 3), lse.transpose(1, 0, 2),
-            dq.transpose(1, 0, 2, 3), dk.sum(axis=0, keepdims=True),
-            dv.sum(axis=0, keepdims=True))
+    # Whole key/value groups (a K/V head with every query head that reads
+    # it), all rows: the first group of the first batch entry and the last
+    # group of the last one (only the last when a group holds more than 16
+    # query heads: multi-query groups are whole batch entries).  O, LSE and
+    # dQ are per query head; dK and dV are the group's sums, so only a whole
+    # group gives them exactly.
+    groups = {(B - 1, Hkv - 1)} if g > 16 else {(0, 0), (B - 1, Hkv - 1)}
+    for b, kvh in sorted(groups):
+        hs = slice(kvh * g, (kvh + 1) * g)
+        sub = {"q": inp["q"][b:b + 1, hs], "do": inp["do"][b:b + 1, hs],
+               "k": inp["k"][b:b + 1, kvh:kvh + 1],
+               "v": inp["v"][b:b + 1, kvh:kvh + 1]}
+        tag = "%s b=%d kvh=%d" % (name, b, kvh)
+        o_ref, lse_ref = oracle.fwd_ext(sub["q"], sub["k"], sub["v"], causal,
+                                        scale, window)
+        check_forward(got["o"][b:b + 1, hs], got["lse"][b:b + 1, hs], o_ref,
+                      lse_ref, tag)
+        del o_ref, lse_ref
+        dq, dk, dv = oracle.bwd_ext(sub["q"], sub["k"], sub["v"], sub["do"],
+                                    causal, scale, window)
+        check_grad("dq", got["dq"][b:b + 1, hs], dq, tag)
+        check_grad("dk", got["dk"][b:b + 1, kvh:kvh + 1], dk, tag)
+        check_grad("dv", got["dv"][b:b + 1, kvh:kvh + 1], dv, tag)

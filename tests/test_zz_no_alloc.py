@@ -3,8 +3,10 @@
 Callers that cannot allocate device memory use fa_bwd_noalloc, which runs the
 same kernels as fa_bwd with the library's fixed device scratch array in place
 of a caller workspace.  This checks, through the C ABI, that two calls in a
-row give the same gradients as fa_bwd (within the backward tolerance), and
-that shapes whose scratch would exceed the fixed maximum are refused.
+row give the same gradients as fa_bwd (within the backward tolerance), that
+its gradients match the CPU fp64 oracle on their own, also after a call of
+another shape has left its own values in the shared scratch, and that shapes
+whose scratch would exceed the fixed maximum are refused.
 
 The file is named so that pytest collects it last.
 """
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tiled_attention_bwd_gb300 import fa
 from tiled_attention_bwd_gb300.workloads import default_scale, make_inputs
 
@@ -44,6 +47,31 @@ def test_noalloc_backward_matches_workspace_backward(B, H, N, d, causal):
         for g, r in zip(got, ref):
             assert torch.isfinite(g.float()).all()
             assert _rel_fro(g, r) <= GRAD_REL_FRO
+
+
+@pytest.mark.gpu
+def test_noalloc_backward_matches_oracle_across_shapes():
+    # Shape A, then shape B (a different layout of the shared scratch), then
+    # shape A again: each call's gradients are checked against the oracle,
+    # so nothing a previous call left in the scratch may leak into them.
+    dev = torch.device("cuda:0")
+    shapes = [(2, 3, 333, 128, True), (1, 2, 700, 64, False),
+              (2, 3, 333, 128, True)]
+    for x, (B, H, N, d, causal) in enumerate(shapes):
+        inp = make_inputs(B, H, N, d, seed=500 + N)
+        q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+        scale = default_scale(d)
+        o, lse = fa.fa_fwd(q, k, v, causal, scale)
+        got = tuple(torch.full_like(q, float("nan")) for _ in range(3))
+        fa.fa_bwd_noalloc(q, k, v, o, lse, do, causal, scale, *got)
+        assert fa.fa_check_device_status(dev) == 0
+        refs = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], causal,
+                          scale)
+        for name, g, r in zip(("dq", "dk", "dv"), got, refs):
+            g = g.double().cpu().numpy()
+            assert np.isfinite(g).all(), (x, name)
+            rf = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+            assert rf <= GRAD_REL_FRO, (x, name, rf)
 
 
 @pytest.mark.gpu
