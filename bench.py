@@ -2,13 +2,21 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--hkv HKV] [--window W] [--varlen] [--fp8]
-                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+                    [--impl ours|reference] [--replicas] [--no-e2e]
+                    [--no-cpu-baseline]
 
 One step = fa_fwd + fa_bwd over the whole workload (default: 4x64x4096x128
-causal, the headline shape), inputs resident in HBM.  Each rank runs the full
-workload on its own GPU (weak scaling, no collective on the data path); the
-reported value is the total algorithmic FLOPs of all ranks divided by the
-slowest rank's time.  Rank 0 prints one JSON line.
+causal, the headline shape), inputs resident in HBM.  With several GPUs each
+rank takes a contiguous range of the workload's key/value groups (whole
+batch entries with --varlen) and runs the plain entry points on it, with no
+collective on the data path (strong scaling); --replicas runs the whole
+workload on every rank instead (weak scaling).  The reported value is the
+algorithmic FLOPs of all ranks divided by the slowest rank's time.  Rank 0
+prints one JSON line, with per-kernel rooflines (forward, backward pre, main
+and post kernels, each timed by CUDA events on the launching stream) and the
+CPU oracle timed on the host cores: on a sample of this workload, on a
+sample of every workload (full-workload time extrapolated), and on the
+smallest workload with one core.
 
 FLOP convention: forward = 4 B H N^2 d (halved when causal), backward = 2.5 x
 forward, step = 3.5 x forward.  With --window the N^2 (or N^2 / 2) becomes
@@ -200,6 +208,17 @@ def step_flops(w, window, lens=None):
     return f, 2.5 * f
 
 
+def slice_flops(w, window, sh, lens=None):
+    """Algorithmic forward and backward FLOPs of one rank's slice `sh` of
+    workload w (a HeadSlice); with per-sequence lengths the slice holds
+    whole batch entries and counts their own visible pairs."""
+    if lens is not None:
+        return step_flops(w, window, lens[sh.b_lo:sh.b_hi])
+    f, b = step_flops(w, window, None)
+    frac = (sh.q_hi - sh.q_lo) / float(w.B * w.H)
+    return f * frac, b * frac
+
+
 def bench_lengths(w):
     """Per-sequence lengths of --varlen: uniform over [1, N], seeded."""
     from tiled_attention_bwd_gb300.workloads import make_seq_lens
@@ -253,6 +272,79 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def pre_post_bytes(B, H, Hkv, N, d, lens=None):
+    """Algorithmic DRAM bytes of the backward's two row passes (None with
+    per-sequence lengths).  pre: reads O, dO (2 d bytes each per row) and
+    LSE (4), writes D and -LSE log2 e (4 + 4 per padded row) and clears the
+    fp32 dQ accumulator (4 d); with a key/value group split over blocks (more
+    than 8 query heads per key/value head) also clears the fp32 dK, dV
+    accumulators.  post: reads the dQ accumulator (4 d), writes dQ (2 d);
+    with a split group also reads the dK, dV accumulators, writes dK, dV."""
+    if lens is not None:
+        return None, None
+    rows = B * H * N
+    n_pad = (N + 127) // 128 * 128
+    kv_rows = B * Hkv * N if H // Hkv > 8 else 0
+    pre = rows * (4 * d + 4 + 4 * d) + B * H * n_pad * 8 + kv_rows * 8 * d
+    post = rows * 6 * d + kv_rows * 12 * d
+    return float(pre), float(post)
+
+
+def oracle_whole_heads(w, heads, window=-1):
+    """Oracle forward + backward on `heads` whole heads (every row) of
+    workload w, in the order of the workload's own inputs.  Returns
+    (algorithmic FLOPs, seconds)."""
+    import oracle
+    from tiled_attention_bwd_gb300.workloads import make_inputs, visible_pairs
+    inp = make_inputs(w.B, w.H, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    flat = {n: inp[n].reshape(w.B * w.H, w.N, w.d)[:heads].double().numpy()
+            for n in ("q", "k", "v", "do")}
+    del inp
+    t0 = time.perf_counter()
+    oracle.fwd(flat["q"], flat["k"], flat["v"], w.causal, w.scale)
+    oracle.bwd(flat["q"], flat["k"], flat["v"], flat["do"], w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    pairs = float(visible_pairs(w.N, w.causal, window))
+    return heads * pairs * 4.0 * w.d * 3.5, dt
+
+
+def cpu_baselines(w, window):
+    """The oracle timed on the host: the workload's own sample (`main`),
+    every workload on a bounded sample of whole heads with the full-workload
+    time extrapolated (`configs`), and the smallest workload on one core."""
+    import oracle
+    from tiled_attention_bwd_gb300.workloads import WORKLOADS, visible_pairs
+    cores = oracle.num_threads()
+    heads = min(w.B * w.H, 2 * cores)
+    f, s_ = oracle_sample(w, heads, w.N, window)
+    main = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "all %d query rows of %d heads of %s, fwd+bwd, %.1f s"
+                      % (w.N, heads, w.name, s_)}
+    configs = []
+    for c in WORKLOADS.values():
+        per_head = visible_pairs(c.N, c.causal, -1) * 4.0 * c.d * 3.5
+        hs = int(max(1, min(c.B * c.H, round(6e10 / per_head))))
+        f, s_ = oracle_whole_heads(c, hs)
+        configs.append({
+            "workload": c.name, "value": f / s_ / 1e12, "unit": "TFLOP/s",
+            "cores": cores, "heads_sampled": hs, "heads_total": c.B * c.H,
+            "seconds": s_,
+            "full_workload_seconds": s_ * (c.B * c.H) / hs,
+            "full_workload_seconds_kind": ("measured" if hs == c.B * c.H
+                                           else "extrapolated")})
+    small = WORKLOADS["small_2x8x512x64"]
+    oracle.set_num_threads(1)
+    try:
+        f, s_ = oracle_whole_heads(small, small.B * small.H)
+    finally:
+        oracle.set_num_threads(cores)
+    one = {"workload": small.name, "value": f / s_ / 1e12, "unit": "TFLOP/s",
+           "cores": 1, "seconds": s_, "heads": small.B * small.H,
+           "sample": "the whole workload, fwd+bwd"}
+    return main, configs, one
+
+
 def run_ours(args, w, rank, world, local):
     import torch
     from tiled_attention_bwd_gb300 import (fa_bwd_ext, fa_bwd_set_phase_events,
@@ -260,6 +352,8 @@ def run_ours(args, w, rank, world, local):
                                            fa_bwd_varlen,
                                            fa_check_device_status, fa_fwd_ext,
                                            fa_fwd_varlen, load_library)
+    from tiled_attention_bwd_gb300.shard import (full_slice, head_slice,
+                                                 slice_heads)
     from tiled_attention_bwd_gb300.workloads import make_grouped_inputs
 
     load_library()
@@ -272,27 +366,48 @@ def run_ours(args, w, rank, world, local):
     hkv = w.H if args.hkv is None else args.hkv
     window = args.window
     inp_cpu = make_grouped_inputs(w.B, w.H, hkv, w.N, w.d, w.seed, w.qk_mult)
-    q, k, v, do = (inp_cpu[n].to(dev) for n in ("q", "k", "v", "do"))
+    lens_all = bench_lengths(w) if args.varlen else None
+    # This rank's share: whole key/value groups (whole batch entries with
+    # lengths) of the one problem, or, with --replicas, all of it.
+    if args.replicas or world == 1:
+        sh = full_slice(w.B, w.H, hkv)
+    else:
+        sh = head_slice(rank, world, w.B, w.H, hkv, by_batch=args.varlen)
+    Bs, Hs, Hkvs = sh.B_s, sh.H_s, sh.Hkv_s
+    part = {n: slice_heads(inp_cpu[n], sh.q_lo, sh.q_hi, Bs) if n in ("q", "do")
+            else slice_heads(inp_cpu[n], sh.kv_lo, sh.kv_hi, Bs)
+            for n in ("q", "k", "v", "do")}
+    part = {n: t.contiguous() for n, t in part.items()}
+    del inp_cpu
+    q, k, v, do = (part[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     dq = torch.empty_like(q)
     dk, dv = torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(fa_bwd_ext_workspace_size(w.B, w.H, hkv, w.N, w.d),
+    ws = torch.empty(max(1, fa_bwd_ext_workspace_size(Bs, Hs, Hkvs, w.N, w.d)),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    lens_cpu = bench_lengths(w) if args.varlen else None
+    lens_cpu = lens_all[sh.b_lo:sh.b_hi] if args.varlen else None
     sl = lens_cpu.to(dev) if args.varlen else None
-    fwd_flops, bwd_flops = step_flops(w, window, lens_cpu)
+    # FLOPs of the whole problem (all ranks) and of this rank's share.
+    fwd_all, bwd_all = step_flops(w, window, lens_all)
+    if args.replicas:
+        fwd_all, bwd_all = world * fwd_all, world * bwd_all
+    fwd_flops, bwd_flops = slice_flops(w, window, sh, lens_all)
+    idle = sh.empty
 
     def fwd():
+        if idle:
+            return
         if sl is None:
             fa_fwd_ext(q, k, v, w.causal, w.scale, window, out=o, lse=lse)
         else:
             fa_fwd_varlen(q, k, v, sl, w.causal, w.scale, window, out=o,
                           lse=lse)
 
-    def step():
-        fwd()
+    def bwd():
+        if idle:
+            return
         if sl is None:
             fa_bwd_ext(q, k, v, o, lse, do, w.causal, w.scale, window, dq=dq,
                        dk=dk, dv=dv, workspace=ws)
@@ -300,22 +415,32 @@ def run_ours(args, w, rank, world, local):
             fa_bwd_varlen(q, k, v, o, lse, do, sl, w.causal, w.scale, window,
                           dq=dq, dk=dk, dv=dv, workspace=ws)
 
+    def step():
+        fwd()
+        bwd()
+
     for _ in range(args.warmup):
         step()
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    # -------- timed region: whole step, plus the backward main kernel alone
+    # -------- timed region: whole steps.  Events on the launching stream
+    # also mark each backward call and its main kernel, so the three
+    # backward launches are timed one by one (pre: call start to main start;
+    # post: main end to call end).
     K = args.steps
-    main_ev = [(torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+
+    def ev_pair():
+        return (torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True))
+    main_ev = [ev_pair() for _ in range(K)]
+    bwd_ev = [ev_pair() for _ in range(K)]
     # torch creates the CUDA event lazily and only times events it recorded
     # itself: record each once here; the library re-records them later.
     for a, b in main_ev:
         a.record(stream)
         b.record(stream)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    t_start, t_end = ev_pair()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -324,7 +449,10 @@ def run_ours(args, w, rank, world, local):
     t_start.record(stream)
     for i in range(K):
         fa_bwd_set_phase_events(*main_ev[i])
-        step()
+        fwd()
+        bwd_ev[i][0].record(stream)
+        bwd()
+        bwd_ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -333,12 +461,18 @@ def run_ours(args, w, rank, world, local):
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error in the timed region")
     step_ms_local = t_start.elapsed_time(t_end) / K
-    main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / K
+    if idle:
+        main_ms = pre_ms = post_ms = 0.0
+    else:
+        main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / K
+        pre_ms = sum(bwd_ev[i][0].elapsed_time(main_ev[i][0])
+                     for i in range(K)) / K
+        post_ms = sum(main_ev[i][1].elapsed_time(bwd_ev[i][1])
+                      for i in range(K)) / K
     step_ms = max_over_ranks(step_ms_local, world, dev)
 
     # -------- forward alone (same inputs), for the forward-only figure
-    fw_s = torch.cuda.Event(enable_timing=True)
-    fw_e = torch.cuda.Event(enable_timing=True)
+    fw_s, fw_e = ev_pair()
     for _ in range(max(1, args.warmup)):
         fwd()
     torch.cuda.synchronize(dev)
@@ -347,19 +481,19 @@ def run_ours(args, w, rank, world, local):
         fwd()
     fw_e.record(stream)
     torch.cuda.synchronize(dev)
-    fwd_ms = max_over_ranks(fw_s.elapsed_time(fw_e) / K, world, dev)
+    fwd_ms_local = fw_s.elapsed_time(fw_e) / K
+    fwd_ms = max_over_ranks(fwd_ms_local, world, dev)
 
     # -------- FP8 forward (optional): Q, K quantised to E4M3 inside the call
     fp8 = None
-    if args.fp8:
+    if args.fp8 and not idle:
         from tiled_attention_bwd_gb300 import fa_fwd_fp8, fa_fwd_fp8_workspace_size
-        ws8 = torch.empty(fa_fwd_fp8_workspace_size(w.B, w.H, w.N, w.d),
+        ws8 = torch.empty(fa_fwd_fp8_workspace_size(Bs, Hs, w.N, w.d),
                           dtype=torch.uint8, device=dev)
         for _ in range(max(3, args.warmup)):
             fa_fwd_fp8(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws8)
         torch.cuda.synchronize(dev)
-        f8_s = torch.cuda.Event(enable_timing=True)
-        f8_e = torch.cuda.Event(enable_timing=True)
+        f8_s, f8_e = ev_pair()
         f8_s.record(stream)
         for _ in range(K):
             fa_fwd_fp8(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws8)
@@ -368,7 +502,7 @@ def run_ours(args, w, rank, world, local):
         if fa_check_device_status(dev) != 0:
             raise RuntimeError("device status error in the FP8 forward")
         f8_ms = max_over_ranks(f8_s.elapsed_time(f8_e) / K, world, dev)
-        fp8 = {"value": world * fwd_flops / (f8_ms * 1e-3) / 1e12,
+        fp8 = {"value": fwd_all / (f8_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "ms": f8_ms,
                "note": "fa_fwd_fp8: E4M3 quantisation of Q and K (two "
                        "launches) + forward with Q K^T on FP8 tensor cores; "
@@ -377,10 +511,10 @@ def run_ours(args, w, rank, world, local):
     # -------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        host = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
-        outs = {n: torch.empty_like(host["q"]).pin_memory()
+        host = {n: part[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {n: torch.empty_like(host["q" if n in ("o", "dq") else "k"]).pin_memory()
                 for n in ("o", "dq", "dk", "dv")}
-        lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        lse_h = torch.empty(tuple(q.shape[:3]), dtype=torch.float32).pin_memory()
 
         if sl is not None:
             host["seq_lens"] = lens_cpu.pin_memory()
@@ -404,10 +538,13 @@ def run_ours(args, w, rank, world, local):
                                                    fa_step_host_scratch_size)
             mode = "fa_step_host (pinned host buffers, pipelined by head chunks)"
             scratch = torch.empty(
-                fa_step_host_scratch_size(w.B, w.H, w.N, w.d, args.chunk_heads),
+                max(1, fa_step_host_scratch_size(Bs, Hs, w.N, w.d,
+                                                 args.chunk_heads)),
                 dtype=torch.uint8, device=dev)
 
             def e2e_step():
+                if idle:
+                    return
                 fa_step_host(host["q"], host["k"], host["v"], host["do"],
                              w.causal, w.scale, outs["o"], lse_h, outs["dq"],
                              outs["dk"], outs["dv"], scratch=scratch,
@@ -417,7 +554,7 @@ def run_ours(args, w, rank, world, local):
             e2e_step()
         torch.cuda.synchronize(dev)
         barrier(world)
-        s, e = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        s, e = ev_pair()
         K_e2e = max(3, K // 4)
         s.record(stream)
         for _ in range(K_e2e):
@@ -429,57 +566,90 @@ def run_ours(args, w, rank, world, local):
         h2d = sum(host[n].numel() * host[n].element_size() for n in host)
         d2h = (sum(outs[n].numel() * outs[n].element_size() for n in outs)
                + lse_h.numel() * 4)
-        e2e = {"value": world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12,
+        e2e = {"value": (fwd_all + bwd_all) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "mode": mode}
 
-    traffic = committed_traffic("bwd_main_kernel")
-    traffic_bytes = (traffic[0] if traffic and traffic[1] == w.name
-                     and not variant_config(w, args) else None)
-    value = world * (fwd_flops + bwd_flops) / (step_ms * 1e-3) / 1e12
-    fwd_tflops = world * fwd_flops / (fwd_ms * 1e-3) / 1e12
-    main_tflops = bwd_flops / (main_ms * 1e-3) / 1e12
+    plain = not variant_config(w, args)
 
-    cpu = None
+    def traffic_of(kernel):
+        t = committed_traffic(kernel)
+        return (t[0] if t and t[1] == w.name and plain and world == 1
+                else None)
+
+    value = (fwd_all + bwd_all) / (step_ms * 1e-3) / 1e12
+    fwd_tflops = fwd_all / (fwd_ms * 1e-3) / 1e12
+    pre_b, post_b = pre_post_bytes(Bs, Hs, Hkvs, w.N, w.d, lens_cpu)
+
+    def tensor_roof(kernel, flop, ms, peak, peak_note):
+        a_ = flop / (ms * 1e-3) / 1e12 if ms > 0 else None
+        return {"kernel": kernel, "bound": "tensor", "achieved": a_,
+                "peak": peak, "unit": "TFLOP/s",
+                "frac": a_ / peak if a_ is not None else None,
+                "peak_source": peak_note, "ms_per_launch": ms,
+                "traffic": traffic_of(kernel),
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
+                "algorithmic_flop_per_launch": flop}
+
+    def hbm_roof(kernel, nbytes, ms):
+        if nbytes is None or ms <= 0:
+            return None
+        a_ = nbytes / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": a_,
+                "peak": hbm_peak, "unit": "GB/s", "frac": a_ / hbm_peak,
+                "peak_source": "%s copy bandwidth" % peak_src,
+                "ms_per_launch": ms, "traffic": traffic_of(kernel),
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
+                "algorithmic_bytes_per_launch": nbytes}
+
+    burst_note = ("%s bf16 burst (each kernel is timed per launch at the "
+                  "maximum clock, not in a power-capped loop)" % peak_src)
+    roofline = tensor_roof("bwd_main_kernel", bwd_flops, main_ms, peak_burst,
+                           burst_note)
+    rooflines = {
+        "fwd_kernel": tensor_roof("fwd_kernel", fwd_flops, fwd_ms_local,
+                                  peak_burst, burst_note),
+        "bwd_pre_kernel": hbm_roof("bwd_pre_kernel", pre_b, pre_ms),
+        "bwd_post_kernel": hbm_roof("bwd_post_kernel", post_b, post_ms),
+    }
+
+    cpu = cpu_configs = cpu_one = None
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        cores = oracle.num_threads()
-        heads = 2 * cores          # about 10 s of fp64 work at 4096x128
-        f, s_ = oracle_sample(w, heads, w.N, window)
-        cpu = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": cores,
-               "kind": "oracle",
-               "sample": "all %d query rows of %d heads of %s, fwd+bwd, "
-                         "%.1f s" % (w.N, heads, w.name, s_)}
+        cpu, cpu_configs, cpu_one = cpu_baselines(w, window)
 
     if rank != 0:
         return
+    if args.replicas:
+        per_gpu, scaling = "full workload per rank (replicas)", "weak"
+    else:
+        per_gpu = ("contiguous key/value groups of the one workload per rank"
+                   if not args.varlen else
+                   "contiguous batch entries of the one workload per rank")
+        scaling = "strong"
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": scaling,
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
                         "d": w.d, "causal": w.causal, "scale": w.scale,
                         "qk_mult": w.qk_mult,
-                        "per_gpu": "full workload per rank",
+                        "per_gpu": per_gpu,
                         "l2": "inputs larger than L2 (%d MB per Q tensor)" % (
-                            q.numel() * 2 // 2**20)},
+                            w.B * w.H * w.N * w.d * 2 // 2**20)},
                        **variant_config(w, args)),
         "fwd": {"value": fwd_tflops, "unit": "TFLOP/s", "ms": fwd_ms,
                 "frac_of_peak": fwd_tflops / world / peak_burst},
         "fwd_bwd_frac_of_peak": value / world / peak_burst,
         "peak": {"bf16_tflops": peak_burst, "bf16_tflops_sustained": peak_sust,
-                 "source": peak_src},
-        "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor",
-                     "achieved": main_tflops, "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": main_tflops / peak_burst,
-                     "peak_source": "%s bf16 burst (clocks stay at max: "
-                                    "not power-capped)" % peak_src,
-                     "ms_per_launch": main_ms, "traffic": traffic_bytes,
-                     "traffic_unit": "bytes per launch (ncu dram read+write)",
-                     "algorithmic_flop_per_launch": bwd_flops},
+                 "hbm_gbs": hbm_peak, "source": peak_src},
+        "roofline": roofline,
+        "rooflines": rooflines,
+        "bwd_ms": {"pre": pre_ms, "main": main_ms, "post": post_ms},
         "cpu_baseline": cpu,
+        "cpu_baseline_configs": cpu_configs,
+        "cpu_baseline_1core": cpu_one,
         "e2e": e2e,
         "fwd_fp8": fp8,
         "gpu_launches": 4 * K,
@@ -506,6 +676,9 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="also time the FP8 forward (fa_fwd_fp8)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--replicas", action="store_true",
+                    help="with several GPUs, run the whole workload on every "
+                         "rank instead of splitting its heads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

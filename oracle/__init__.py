@@ -89,6 +89,8 @@ def _load():
         lib.oracle_bwd_ext_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
@@ -115,6 +117,13 @@ def _shape(q):
 def num_threads() -> int:
     """OpenMP threads the oracle runs with (OMP_NUM_THREADS, else all cores)."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Run later oracle calls (from this thread) on n >= 1 threads."""
+    if int(n) < 1:
+        raise ValueError("thread count must be >= 1")
+    _load().oracle_set_num_threads(int(n))
 
 
 def fwd(q, k, v, causal: bool, scale: float):

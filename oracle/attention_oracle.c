@@ -50,6 +50,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads of the later calls made from this thread (n >= 1). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 static double dot(const double* a, const double* b, int64_t d) {
   double s = 0.0;
   for (int64_t t = 0; t < d; ++t) s += a[t] * b[t];
