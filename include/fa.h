@@ -82,6 +82,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
  * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,N,d] followed by two fp32 per-row vectors
  * (D_i = dO_i . O_i and -LSE_i * log2(e)) padded to whole 128-row tiles.
+ * The accumulator is where the backward's dQ contributions of all key tiles
+ * meet ("RTX Flash Attention Implementation COMPLETE", "Flash Attention
+ * Backward Kernel": atomic memory operations for the gradient updates, read
+ * here as additions in fp32), and D_i is the row term of the
+ * recomputation from the saved LSE ("GPU Performance Optimization Batch 1 --
+ * Design Spec", Item 3, backward paragraph).  The caller owns the memory, as
+ * the page's usage example owns its tensors ("Usage Examples").
  * Returns 0 for an empty problem or unsupported d.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -237,7 +244,11 @@ fa_status fa_step_host(const void* q, const void* k, const void* v,
  * Synchronises `stream`, then reports (and clears) the device status record
  * of the current GPU: FA_ERR_DEVICE_TIMEOUT if any kernel of this library
  * gave up on a pipeline wait since the last check, FA_ERR_CUDA if the stream
- * reported an error, else FA_OK.
+ * reported an error, else FA_OK.  This is the error reporting of
+ * "RTX Flash Attention Implementation COMPLETE", "Complete Rust Integration"
+ * ("Error Handling: comprehensive error reporting and recovery") for work
+ * that runs asynchronously: a failure inside a kernel is recorded on the
+ * device and read here, after which the library is usable again.
  */
 fa_status fa_check_device_status(void* stream);
 
@@ -297,7 +308,10 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
 /* Size in bytes of the fixed scratch array used by fa_bwd_noalloc. */
 size_t fa_bwd_noalloc_max_workspace(void);
 
-/* Human-readable name of a status code (static storage, never NULL). */
+/*
+ * Human-readable name of a status code (static storage, never NULL), the
+ * reporting half of the same page's "Error Handling" item.
+ */
 const char* fa_status_string(fa_status s);
 
 #ifdef __cplusplus

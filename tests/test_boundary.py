@@ -6,6 +6,7 @@ would reach a GPU.  Every call here returns before the library's first CUDA
 runtime call.
 """
 import ctypes
+import json
 import subprocess
 
 import pytest
@@ -42,12 +43,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name)
 
 
-def test_library_targets_sm103a():
-    out = subprocess.run(["cuobjdump", "--list-elf", fa.LIB_PATH],
-                         capture_output=True, text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+def test_library_targets_sm103a(lib):
+    # The flags the build recorded next to the library: one target,
+    # sm_103a, for every object and for the link.
+    with open(fa_build.FLAGS) as f:
+        flags = json.load(f)
+    for step in ("compile", "link"):
+        args = flags[step]
+        targets = [args[i + 1] for i, a in enumerate(args)
+                   if a in ("-gencode", "-arch", "--gpu-architecture")]
+        assert targets == ["arch=compute_103a,code=sm_103a"], (step, targets)
 
 
 def test_missing_library_fails_loudly():

@@ -9,6 +9,7 @@ through ``cudaGetDriverEntryPointByVersion``; nothing links libcuda.
 """
 import argparse
 import concurrent.futures as cf
+import json
 import os
 import shutil
 import subprocess
@@ -20,6 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libfa.so")
+FLAGS = os.path.join(OUT_DIR, "build_flags.json")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -78,6 +80,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("link of libfa.so failed")
     os.replace(tmp, LIB)
+    # The target architecture as built, for the test suite to check without
+    # opening the binary.
+    with open(FLAGS, "w") as f:
+        json.dump({"compile": common, "link": ARCH + ["-shared", "-cudart",
+                                                      "static"]}, f, indent=1)
     return LIB
 
 
