@@ -81,7 +81,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
 /*
  * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,N,d] followed by two fp32 per-row vectors
- * (D_i = dO_i . O_i and -LSE_i * log2(e)) padded to whole 128-row tiles.
+ * (D_i = dO_i . O_i and -LSE_i * log2(e)) padded to whole 128-row tiles and
+ * a 256-byte counter that hands the work out to the thread blocks.
  * The accumulator is where the backward's dQ contributions of all key tiles
  * meet ("RTX Flash Attention Implementation COMPLETE", "Flash Attention
  * Backward Kernel": atomic memory operations for the gradient updates, read

@@ -126,7 +126,8 @@ def _align(x, a=256):
                                      (1, 1, 1, 64), (3, 5, 333, 128)])
 def test_workspace_size(lib, B, H, N, d):
     n_pad = _align(N, 128)
-    expect = (_align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4))
+    # dQ accumulator, D and -LSE log2(e) per padded row, the work counter
+    expect = (_align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4) + 256)
     assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
     assert fa.fa_bwd_workspace_size(B, H, N, d) == expect
 
@@ -172,7 +173,7 @@ def test_grouped_head_argument_checks(lib):
                                          (1, 16, 2, 1000, 128)])
 def test_grouped_workspace_size(lib, B, H, Hkv, N, d):
     n_pad = _align(N, 128)
-    base = _align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4)
+    base = _align(B * H * N * d * 4) + 2 * _align(B * H * n_pad * 4) + 256
     g = H // Hkv
     hpb = max(h for h in range(1, min(g, 8) + 1) if g % h == 0)
     extra = 2 * _align(B * Hkv * N * d * 4) if g // hpb > 1 else 0

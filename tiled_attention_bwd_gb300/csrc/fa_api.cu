@@ -190,12 +190,13 @@ int heads_per_block(int qgroup) {
 }
 
 struct WsLayout {
-  size_t dq_acc_off, ddot_off, lse2_off, dk_acc_off, dv_acc_off, total;
+  size_t dq_acc_off, ddot_off, lse2_off, sched_off, dk_acc_off, dv_acc_off, total;
   int hpb, nsplit;
 };
 
-// dQacc [B,H,N,d] | D [B*H, N_pad] | LSE2 [B*H, N_pad] (| dKacc, dVacc
-// [B,Hkv,N,d] when the group is split), each 256-byte aligned.
+// dQacc [B,H,N,d] | D [B*H, N_pad] | LSE2 [B*H, N_pad] | the main kernel's
+// work counter (256 bytes) (| dKacc, dVacc [B,Hkv,N,d] when the group is
+// split), each 256-byte aligned.
 WsLayout ws_layout(int B, int H, int Hkv, int N, int d) {
   const size_t BH = (size_t)B * H, BHkv = (size_t)B * Hkv;
   const size_t n_pad = align_up((size_t)N, fa::kTile);
@@ -206,7 +207,8 @@ WsLayout ws_layout(int B, int H, int Hkv, int N, int d) {
   w.dq_acc_off = 0;
   w.ddot_off = align_up(BH * N * d * sizeof(float), 256);
   w.lse2_off = w.ddot_off + align_up(BH * n_pad * sizeof(float), 256);
-  w.dk_acc_off = w.lse2_off + align_up(BH * n_pad * sizeof(float), 256);
+  w.sched_off = w.lse2_off + align_up(BH * n_pad * sizeof(float), 256);
+  w.dk_acc_off = w.sched_off + 256;
   const size_t kv_acc = w.nsplit > 1 ? align_up(BHkv * N * d * sizeof(float), 256) : 0;
   w.dv_acc_off = w.dk_acc_off + kv_acc;
   w.total = w.dv_acc_off + kv_acc;
@@ -383,6 +385,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.dk_acc = reinterpret_cast<float*>(ws + w.dk_acc_off);
+  a.work_next = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   a.dv_acc = reinterpret_cast<float*>(ws + w.dv_acc_off);
   a.hpb = w.hpb;
   a.nsplit = w.nsplit;
@@ -408,7 +411,8 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   if (e == cudaSuccess && g_ev_before_main)
     e = cudaEventRecord(g_ev_before_main, st);
   if (e == cudaSuccess)
-    e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, a, d, causal != 0, st);
+    e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, a, d, causal != 0,
+                            ctx->sm_count, st);
   if (e == cudaSuccess && g_ev_after_main)
     e = cudaEventRecord(g_ev_after_main, st);
   if (e == cudaSuccess) e = fa::launch_bwd_post(a, d, elem_blocks, st);

@@ -12,7 +12,8 @@
 //   pre   D_i and LSE2_i = -LSE_i*log2(e) per row (padded to whole tiles:
 //         D = 0 and LSE2 = -inf past N, which zeroes P there); dQ
 //         accumulator := 0.
-//   main  one thread block per (batch, head, 128-key tile j).  K_j, V_j stay
+//   main  persistent, one thread block per SM walking work items (batch,
+//         head, 128-key tile j).  K_j, V_j stay
 //         in smem; dK_j, dV_j accumulate in TMEM; Q_i (two stages) and dO_i
 //         (one buffer) stream in by TMA (causal: only i >= j).  Per Q tile, five tcgen05
 //         MMAs: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P^T from TMEM),
@@ -72,7 +73,10 @@ struct BwdLayout {
 };
 
 struct BwdBars {
-  uint64_t kv_full;
+  uint64_t k_full;      // K_j of the block's current work item landed
+  uint64_t v_full;      // V_j landed
+  uint64_t k_empty;     // the item's last MMA reading K_j is done
+  uint64_t v_empty;     // the item's last MMA reading V_j is done
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t do_full;
@@ -84,8 +88,12 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t ds_free;
-  uint64_t acc_done;
+  uint64_t acc_done;    // the item's dK_j, dV_j are complete in TMEM
+  uint64_t acc_free;    // ... and have been read out (8 warps arrive)
   uint64_t mma_done;
+  uint64_t sched_full[2];   // work item t published in sched_item[t % 2]
+  uint64_t sched_empty[2];  // ... and read by the MMA thread and 8 warps
+  int sched_item[2];
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -93,6 +101,13 @@ struct BwdBars {
 enum : uint32_t {
   kWBwdProdQEmpty = 0x111,
   kWBwdProdDoEmpty = 0x112,
+  kWBwdProdKEmpty = 0x113,
+  kWBwdProdVEmpty = 0x114,
+  kWBwdProdSched = 0x115,
+  kWBwdMmaSched = 0x218,
+  kWBwdCmpSched = 0x316,
+  kWBwdDqSched = 0x413,
+  kWBwdMmaAccFree = 0x217,
   kWBwdMmaKV = 0x211,
   kWBwdMmaQ = 0x212,
   kWBwdMmaDqFree = 0x213,
@@ -150,6 +165,96 @@ __device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
   }
 }
 
+// One work item of the main kernel: key tile j of key/value head bkv (one
+// split of its query heads when the group is split), visiting nq (query head,
+// query tile) pairs: query heads qh0 .. qh0 + hpb - 1, each over query tiles
+// i_lo .. i_hi (the tiles whose band reaches key tile j).
+struct BwdItem {
+  int bkv, j, qh0, i_lo, i_hi, nq, len;
+};
+
+// Work item w in the schedule order.  Blocks resident together share a few
+// key/value heads, so their Q/dO tiles and dQ accumulator rows stay in L2;
+// causal key tile 0 (the most query tiles) of each head comes first.
+//
+// A block owns key tile j of key/value head bkv and visits, for each of the
+// H / Hkv query heads that read that head, the query tiles whose band
+// reaches tile j (query i sees key k when k <= i if causal and |i - k| <=
+// window if a window is set); iteration `it` is query head it / nq_head of
+// the group and query tile i_lo + it % nq_head.
+//
+// With many query heads per key/value head (multi-query attention) one item
+// per (key/value head, key tile) is too coarse: the group's query heads are
+// then dealt to nsplit items of hpb heads each, whose partial dK_j, dV_j are
+// summed in fp32 (dk_acc, dv_acc) and rounded afterwards.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ BwdItem bwd_item(int w, int n_tiles, const BwdArgs& a) {
+  BwdItem itm;
+  const TileSlot slot = grouped_slot(w, n_tiles, a.BHkv * a.nsplit, a.group);
+  itm.bkv = slot.bh / a.nsplit;
+  const int split = slot.bh - itm.bkv * a.nsplit;
+  itm.j = slot.tile;
+  const int qgroup = a.H / a.Hkv;
+  itm.qh0 = (itm.bkv / a.Hkv) * a.H + (itm.bkv % a.Hkv) * qgroup + split * a.hpb;
+  // With per-sequence lengths (the VARLEN instantiations; the others keep
+  // none of this arithmetic) only the sequence's own tiles count: a key tile
+  // at or past its end gives the item no work (nq = 0).
+  itm.len = VARLEN ? seq_len_of(a.seq_lens, itm.bkv / a.Hkv, a.N) : a.N;
+  const int tiles_b = VARLEN ? (itm.len + kTile - 1) / kTile : n_tiles;
+  const long long k0 = (long long)itm.j * kTile, k1 = k0 + kTile - 1;
+  itm.i_lo = CAUSAL ? itm.j : ((a.window >= 0 && k0 > a.window)
+                                   ? (int)((k0 - a.window) / kTile) : 0);
+  itm.i_hi = tiles_b - 1;
+  if (a.window >= 0) {
+    const long long h = (k1 + a.window) / kTile;
+    if (h < itm.i_hi) itm.i_hi = (int)h;
+  }
+  itm.nq = (!VARLEN || (itm.j < tiles_b && itm.i_hi >= itm.i_lo))
+               ? a.hpb * (itm.i_hi - itm.i_lo + 1) : 0;
+  return itm;
+}
+
+// Work items are handed out dynamically: block b starts with item b and then
+// takes the next unclaimed one from a counter in the workspace (zeroed by the
+// pre kernel), so blocks that drew light items take more of them and all
+// finish together.  Within a head group the items come heaviest first, and
+// the last items of the whole order are the lightest.  The block's producer
+// thread claims the items and publishes each in a two-slot ring in shared
+// memory, which the other roles read in the same order.
+
+// Item t of this block as published by the producer (n_items or more: none
+// left).  Every thread of the calling warp waits and reads; one arrives.
+template <bool kWarp>
+__device__ __forceinline__ bool sched_take(BwdBars* bars, int t, const WaitCtl& wc,
+                                           uint32_t where, int& w) {
+  const int sl = t & 1;
+  const uint32_t par = (uint32_t)(t >> 1) & 1u;
+  const bool ok = kWarp ? wait_bar_warp(&bars->sched_full[sl], par, wc, where)
+                        : wait_bar(&bars->sched_full[sl], par, wc, where);
+  if (!ok) return false;
+  w = *reinterpret_cast<volatile int*>(&bars->sched_item[sl]);
+  if (kWarp) warp_arrive(&bars->sched_empty[sl]);
+  else mbar_arrive(&bars->sched_empty[sl]);
+  return true;
+}
+
+// Walks (query head, query tile) in iteration order without divisions.
+struct QCursor {
+  int bh, i;
+};
+__device__ __forceinline__ void q_next(QCursor& c, const BwdItem& itm) {
+  if (++c.i > itm.i_hi) {
+    c.i = itm.i_lo;
+    ++c.bh;
+  }
+}
+
+// Persistent: one block per SM takes work items one after another.  The
+// barrier phases run on across items (`g` counts the block's query-tile
+// iterations, `t` its items), so the next item's V, first Q and
+// dO tiles load while the current one finishes, its K as soon as the last
+// MMA reading K_j is done, and its first S^T / dP^T overlap the read-out of
+// the current dK_j, dV_j.
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -164,61 +269,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto* bars = reinterpret_cast<BwdBars*>(smem + L::kBarOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Blocks resident together share a few key/value heads, so their Q/dO
-  // tiles and dQ accumulator rows stay in L2; causal key tile 0 (the most
-  // query tiles) of each head starts first.
-  //
-  // A block owns key tile j of key/value head bkv and visits, for each of the
-  // H / Hkv query heads that read that head, the query tiles whose band
-  // reaches tile j (query i sees key k when k <= i if causal and
-  // |i - k| <= window if a window is set); iteration `it` is query head
-  // it / nq_head of the group and query tile i_lo + it % nq_head.
-  //
-  // With many query heads per key/value head (multi-query attention) one
-  // block per (key/value head, key tile) is too coarse: the group's query
-  // heads are then dealt to nsplit blocks of hpb heads each, whose partial
-  // dK_j, dV_j are summed in fp32 (dk_acc, dv_acc) and rounded afterwards.
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const TileSlot slot =
-      grouped_slot((int)blockIdx.x, n_tiles, a.BHkv * a.nsplit, a.group);
-  const int bkv = slot.bh / a.nsplit;
-  const int split = slot.bh - bkv * a.nsplit;
-  const int j = slot.tile;                        // key tile
-  const int qgroup = a.H / a.Hkv;
-  const int qh0 = (bkv / a.Hkv) * a.H + (bkv % a.Hkv) * qgroup + split * a.hpb;
-  // With per-sequence lengths (the VARLEN instantiations; the others keep
-  // none of this arithmetic) only the sequence's own tiles count: a key tile
-  // at or past its end gives the block no work (nq = 0).
-  const int len = VARLEN ? seq_len_of(a.seq_lens, bkv / a.Hkv, a.N) : a.N;
-  const int tiles_b = VARLEN ? (len + kTile - 1) / kTile : n_tiles;
-  int i_lo, i_hi;
-  {
-    const long long k0 = (long long)j * kTile, k1 = k0 + kTile - 1;
-    i_lo = CAUSAL ? j : ((a.window >= 0 && k0 > a.window)
-                             ? (int)((k0 - a.window) / kTile) : 0);
-    i_hi = tiles_b - 1;
-    if (a.window >= 0) {
-      const long long h = (k1 + a.window) / kTile;
-      if (h < i_hi) i_hi = (int)h;
-    }
-  }
-  const int nq = (!VARLEN || (j < tiles_b && i_hi >= i_lo))
-                     ? a.hpb * (i_hi - i_lo + 1) : 0;
-  // A block with no work (a key tile past its sequence's end) leaves before
-  // any barrier, TMEM or shared-memory setup: with short sequences most
-  // blocks of the grid are such blocks.  The condition is uniform over the
-  // block and nothing has been issued yet.
-  if (VARLEN && nq == 0) return;
-  // Walks (query head, query tile) in iteration order without divisions.
-  struct QCursor {
-    int bh, i;
-  };
-  auto q_next = [&](QCursor& c) {
-    if (++c.i > i_hi) {
-      c.i = i_lo;
-      ++c.bh;
-    }
-  };
+  const int n_items = a.BHkv * a.nsplit * n_tiles;
 
   if (threadIdx.x == 0) {
     uint32_t stop = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
@@ -228,7 +280,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       stop = 1;
     }
     bars->abort = stop;
-    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->k_full, 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->k_empty, 1);
+    mbar_init(&bars->v_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
@@ -243,7 +298,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->dq_free, 4);   // one arrival per warp
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_free, 8);  // dK by warps 0-3, dV by warps 4-7
     mbar_init(&bars->mma_done, 1);
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(&bars->sched_full[sl], 1);
+      mbar_init(&bars->sched_empty[sl], 9);  // MMA thread + 8 warps
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -270,47 +330,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
       prefetch_tmap(&tm_dq);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTileBytes);
-#pragma unroll
-      for (int sb = 0; sb < L::kSub; ++sb) {
-        tma_load_3d(k_s + sb * kSubTileBytes, &tm_k, &bars->kv_full, sb * 64,
-                    j * kTile, bkv);
-        tma_load_3d(v_s + sb * kSubTileBytes, &tm_v, &bars->kv_full, sb * 64,
-                    j * kTile, bkv);
-      }
-      int q_par[2] = {-1, -1}, do_par = -1;
+      // Parity of the last load issued into each buffer (-1: none), so that
+      // a stopping block can wait for its copies in flight.
+      int k_par = -1, v_par = -1, q_par[2] = {-1, -1}, do_par = -1;
       bool ok = true;
-      QCursor cur{qh0, i_lo};
-      for (int it = 0; it < nq; ++it, q_next(cur)) {
-        const int i = cur.i, bh = cur.bh;
-        const int stage = it & 1;
-        const uint32_t sp = (uint32_t)((it >> 1) & 1);
-        // Q_i, LSE2_i, D_i into Q stage it%2
-        ok = wait_bar(&bars->q_empty[stage], sp ^ 1u, wc, kWBwdProdQEmpty);
+      uint32_t g = 0;
+      int w = (int)blockIdx.x;
+      for (int t = 0; ok; ++t) {
+        // Claim the next item with work (with per-sequence lengths some have
+        // none) and publish it; n_items or more tells the others to stop.
+        if (t > 0) w = (int)gridDim.x + (int)atomicAdd(a.work_next, 1u);
+        BwdItem itm;
+        while (w < n_items) {
+          itm = bwd_item<CAUSAL, VARLEN>(w, n_tiles, a);
+          if (!VARLEN || itm.nq > 0) break;
+          w = (int)gridDim.x + (int)atomicAdd(a.work_next, 1u);
+        }
+        ok = wait_bar(&bars->sched_empty[t & 1], ((uint32_t)(t >> 1) & 1u) ^ 1u, wc,
+                      kWBwdProdSched);
         if (!ok) break;
-        uint8_t* qs = smem + L::kQOff + stage * L::kQStageBytes;
-        mbar_arrive_expect_tx(&bars->q_full[stage], L::kTileBytes + 2 * kTile * 4);
+        *reinterpret_cast<volatile int*>(&bars->sched_item[t & 1]) = w;
+        mbar_arrive(&bars->sched_full[t & 1]);
+        if (w >= n_items) break;
+        // V_j as soon as the previous item's last dP^T has read its V.
+        if (t > 0) ok = wait_bar(&bars->v_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdVEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->v_full, L::kTileBytes);
 #pragma unroll
         for (int sb = 0; sb < L::kSub; ++sb)
-          tma_load_3d(qs + sb * kSubTileBytes, &tm_q, &bars->q_full[stage],
-                      sb * 64, i * kTile, bh);
-        const size_t row0 = (size_t)bh * a.N_pad + (size_t)i * kTile;
-        bulk_load(qs + L::kTileBytes, a.lse2 + row0, kTile * 4, &bars->q_full[stage]);
-        bulk_load(qs + L::kTileBytes + kTile * 4, a.ddot + row0, kTile * 4,
-                  &bars->q_full[stage]);
-        q_par[stage] = (int)sp;
-        // dO_i into the single dO buffer
-        ok = wait_bar(&bars->do_empty, (uint32_t)(it & 1) ^ 1u, wc, kWBwdProdDoEmpty);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars->do_full, L::kTileBytes);
+          tma_load_3d(v_s + sb * kSubTileBytes, &tm_v, &bars->v_full, sb * 64,
+                      itm.j * kTile, itm.bkv);
+        v_par = t & 1;
+        QCursor cur{itm.qh0, itm.i_lo};
+        for (int it = 0; it < itm.nq; ++it, ++g, q_next(cur, itm)) {
+          const int i = cur.i, bh = cur.bh;
+          const int stage = (int)(g & 1u);
+          const uint32_t sp = (g >> 1) & 1u;
+          // Q_i, LSE2_i, D_i into Q stage g % 2
+          ok = wait_bar(&bars->q_empty[stage], sp ^ 1u, wc, kWBwdProdQEmpty);
+          if (!ok) break;
+          uint8_t* qs = smem + L::kQOff + stage * L::kQStageBytes;
+          mbar_arrive_expect_tx(&bars->q_full[stage], L::kTileBytes + 2 * kTile * 4);
 #pragma unroll
-        for (int sb = 0; sb < L::kSub; ++sb)
-          tma_load_3d(do_s + sb * kSubTileBytes, &tm_do, &bars->do_full,
-                      sb * 64, i * kTile, bh);
-        do_par = it & 1;
+          for (int sb = 0; sb < L::kSub; ++sb)
+            tma_load_3d(qs + sb * kSubTileBytes, &tm_q, &bars->q_full[stage],
+                        sb * 64, i * kTile, bh);
+          const size_t row0 = (size_t)bh * a.N_pad + (size_t)i * kTile;
+          bulk_load(qs + L::kTileBytes, a.lse2 + row0, kTile * 4, &bars->q_full[stage]);
+          bulk_load(qs + L::kTileBytes + kTile * 4, a.ddot + row0, kTile * 4,
+                    &bars->q_full[stage]);
+          q_par[stage] = (int)sp;
+          // dO_i into the single dO buffer
+          ok = wait_bar(&bars->do_empty, (g & 1u) ^ 1u, wc, kWBwdProdDoEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars->do_full, L::kTileBytes);
+#pragma unroll
+          for (int sb = 0; sb < L::kSub; ++sb)
+            tma_load_3d(do_s + sb * kSubTileBytes, &tm_do, &bars->do_full,
+                        sb * 64, i * kTile, bh);
+          do_par = (int)(g & 1u);
+          if (it == 0) {
+            // K_j once the previous item's last MMA reading K is done (its
+            // first Q and dO are already on their way).
+            if (t > 0) ok = wait_bar(&bars->k_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdKEmpty);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->k_full, L::kTileBytes);
+#pragma unroll
+            for (int sb = 0; sb < L::kSub; ++sb)
+              tma_load_3d(k_s + sb * kSubTileBytes, &tm_k, &bars->k_full,
+                          sb * 64, itm.j * kTile, itm.bkv);
+            k_par = t & 1;
+          }
+        }
       }
       if (!ok) {
-        drain_bar(&bars->kv_full, 0, a.timeout_ns);
+        if (k_par >= 0) drain_bar(&bars->k_full, (uint32_t)k_par, a.timeout_ns);
+        if (v_par >= 0) drain_bar(&bars->v_full, (uint32_t)v_par, a.timeout_ns);
         for (int s = 0; s < 2; ++s)
           if (q_par[s] >= 0)
             drain_bar(&bars->q_full[s], (uint32_t)q_par[s], a.timeout_ns);
@@ -337,8 +432,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t q_km0 = sdesc_sw128(smem_addr(smem + L::kQOff), 16, 1024);
       const uint64_t q_mn0 =
           sdesc_sw128(smem_addr(smem + L::kQOff), kSubTileBytes, 1024);
-      auto q_km = [&](int it) { return sdesc_adv(q_km0, (it & 1) * L::kQStageBytes); };
-      auto q_mn = [&](int it) { return sdesc_adv(q_mn0, (it & 1) * L::kQStageBytes); };
+      auto q_km = [&](uint32_t gi) { return sdesc_adv(q_km0, (gi & 1u) * L::kQStageBytes); };
+      auto q_mn = [&](uint32_t gi) { return sdesc_adv(q_mn0, (gi & 1u) * L::kQStageBytes); };
       auto kstep = [](int s) {  // K-major offset of 16-wide K step s
         return (uint32_t)((s >> 2) * kSubTileBytes + (s & 3) * 32);
       };
@@ -347,9 +442,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // tensor core finishes tile it.  Per iteration the issue order is
       //   dV(it)  S^T(it+1)  dK(it)  dQ(it)  dP^T(it+1)
       // S^T(it+1) may overwrite P^T(it) because dV(it) precedes it in the
-      // tensor core's in-order queue.
-      auto issue_st = [&](int it) {  // S^T = K_j Q_i^T  [keys x queries]
-        const uint64_t qd = q_km(it);
+      // tensor core's in-order queue; the same holds across items.
+      auto issue_st = [&](uint32_t gi) {  // S^T = K_j Q_i^T  [keys x queries]
+        const uint64_t qd = q_km(gi);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s)
           mma_ss(tS, sdesc_adv(k_km, kstep(s)), sdesc_adv(qd, kstep(s)), id_st,
@@ -363,63 +458,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  id_st, s > 0 ? 1u : 0u);
         mma_commit(&bars->dp_full);
       };
-      bool ok = wait_bar(&bars->kv_full, 0, wc, kWBwdMmaKV);
-      if (ok) ok = wait_bar(&bars->q_full[0], 0, wc, kWBwdMmaQ);
-      if (ok) {
+      bool ok = true;
+      uint32_t g = 0;
+      for (int t = 0; ok; ++t) {
+        int w;
+        ok = sched_take<false>(bars, t, wc, kWBwdMmaSched, w);
+        if (!ok || w >= n_items) break;
+        const BwdItem itm = bwd_item<CAUSAL, VARLEN>(w, n_tiles, a);
+        const int nq = itm.nq;
+        const uint32_t tp = (uint32_t)t & 1u;
+        // The item's first S^T and dP^T.  dP^T(0) reuses the columns of the
+        // previous item's last dQ, which the drain warps must have read.
+        ok = wait_bar(&bars->k_full, tp, wc, kWBwdMmaKV);
+        if (ok) ok = wait_bar(&bars->q_full[g & 1u], (g >> 1) & 1u, wc, kWBwdMmaQ);
+        if (!ok) break;
         tc_fence_after();
-        issue_st(0);
-        ok = wait_bar(&bars->do_full, 0, wc, kWBwdMmaDo);
-      }
-      if (ok) {
+        issue_st(g);
+        ok = wait_bar(&bars->v_full, tp, wc, kWBwdMmaKV);
+        if (ok) ok = wait_bar(&bars->do_full, g & 1u, wc, kWBwdMmaDo);
+        if (ok && g > 0) ok = wait_bar(&bars->dq_free, (g - 1u) & 1u, wc, kWBwdMmaDqFree);
+        if (!ok) break;
         tc_fence_after();
         issue_dp();
-      }
-      for (int it = 0; it < nq && ok; ++it) {
-        const uint32_t par = (uint32_t)(it & 1);
-        ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
-        if (!ok) break;
-        tc_fence_after();
-        // dV_j += P^T dO_i   [keys x d], K = queries; P^T from TMEM
-#pragma unroll
-        for (int s = 0; s < kTile / 16; ++s)
-          mma_ts(tDV, tS + s * 8, sdesc_adv(do_mn, s * 2048), id_kv,
-                 (it > 0 || s > 0) ? 1u : 0u);
-        mma_commit(&bars->do_empty);   // dO_i no longer needed
-        if (it + 1 < nq) {
-          ok = wait_bar(&bars->q_full[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1),
-                        wc, kWBwdMmaQ);
+        if (nq == 1) mma_commit(&bars->v_empty);   // V_j no longer read
+        for (int it = 0; it < nq && ok; ++it) {
+          const uint32_t gi = g + (uint32_t)it;
+          const uint32_t par = gi & 1u;
+          ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
+          // dK, dV of the previous item must be out of TMEM before this
+          // item's first products overwrite them.
+          if (ok && it == 0 && t > 0)
+            ok = wait_bar(&bars->acc_free, tp ^ 1u, wc, kWBwdMmaAccFree);
           if (!ok) break;
           tc_fence_after();
-          issue_st(it + 1);
-        }
-        ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
-        if (!ok) break;
-        tc_fence_after();
-        // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T from TMEM (bf16
-        // pairs in the dP^T columns), Q read MN-major
-        const uint64_t qmn = q_mn(it);
+          // dV_j += P^T dO_i   [keys x d], K = queries; P^T from TMEM
 #pragma unroll
-        for (int s = 0; s < kTile / 16; ++s)
-          mma_ts(tDK, tDP + s * 8, sdesc_adv(qmn, s * 2048), id_kv,
-                 (it > 0 || s > 0) ? 1u : 0u);
-        mma_commit(&bars->q_empty[it & 1]);   // Q_i, LSE2_i, D_i released
-        // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
-#pragma unroll
-        for (int s = 0; s < kTile / 16; ++s)
-          mma_ss(tDP, sdesc_adv(ds_mn, s * 2048), sdesc_adv(k_mn, s * 2048), id_q,
-                 s > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free);    // dS_i no longer read
-        if (it + 1 < nq) {
-          // dQ_it occupies the dP columns until the drain warps have read it.
-          ok = wait_bar(&bars->dq_free, par, wc, kWBwdMmaDqFree);
-          if (ok) ok = wait_bar(&bars->do_full, par ^ 1u, wc, kWBwdMmaDo);
+          for (int s = 0; s < kTile / 16; ++s)
+            mma_ts(tDV, tS + s * 8, sdesc_adv(do_mn, s * 2048), id_kv,
+                   (it > 0 || s > 0) ? 1u : 0u);
+          mma_commit(&bars->do_empty);   // dO_i no longer needed
+          if (it + 1 < nq) {
+            ok = wait_bar(&bars->q_full[(gi + 1u) & 1u], ((gi + 1u) >> 1) & 1u,
+                          wc, kWBwdMmaQ);
+            if (!ok) break;
+            tc_fence_after();
+            issue_st(gi + 1u);
+          }
+          ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
           if (!ok) break;
           tc_fence_after();
-          issue_dp();
+          // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T from TMEM (bf16
+          // pairs in the dP^T columns), Q read MN-major
+          const uint64_t qmn = q_mn(gi);
+#pragma unroll
+          for (int s = 0; s < kTile / 16; ++s)
+            mma_ts(tDK, tDP + s * 8, sdesc_adv(qmn, s * 2048), id_kv,
+                   (it > 0 || s > 0) ? 1u : 0u);
+          mma_commit(&bars->q_empty[gi & 1u]);   // Q_i, LSE2_i, D_i released
+          // dQ_i = dS K_j   [queries x d], K = keys; dS read MN-major
+#pragma unroll
+          for (int s = 0; s < kTile / 16; ++s)
+            mma_ss(tDP, sdesc_adv(ds_mn, s * 2048), sdesc_adv(k_mn, s * 2048), id_q,
+                   s > 0 ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+          mma_commit(&bars->ds_free);    // dS_i no longer read
+          if (it + 1 < nq) {
+            // dQ_it occupies the dP columns until the drain warps have read it.
+            ok = wait_bar(&bars->dq_free, par, wc, kWBwdMmaDqFree);
+            if (ok) ok = wait_bar(&bars->do_full, par ^ 1u, wc, kWBwdMmaDo);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp();
+            if (it + 2 == nq) mma_commit(&bars->v_empty);   // V_j no longer read
+          }
         }
+        if (!ok) break;
+        mma_commit(&bars->k_empty);    // K_j no longer read
+        mma_commit(&bars->acc_done);   // dK_j, dV_j complete
+        g += (uint32_t)nq;
       }
-      if (ok) mma_commit(&bars->acc_done);
       mma_commit(&bars->mma_done);
       drain_bar(&bars->mma_done, 0, a.timeout_ns);
     }
@@ -431,139 +548,151 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c = a.scale_log2;
     const uint64_t c2 = bcast2(c);
     bool ok = run;
-    // Band: query q (global) sees key k when dmin <= q - k <= dmax (INT_MIN /
-    // INT_MAX: no bound); a tile pair needs the mask only if its offsets
-    // reach outside [dmin, dmax].  Tile offsets fit in int because
-    // N <= 2^30 and the window is below N.
-    // With per-sequence lengths, key rows past the sequence's end hold real
-    // (finite) data, so their P must be forced to zero: the tile that holds
-    // the end takes the masked path, with no visible query for those rows.
-    const bool key_in = j * kTile + r < len;
-    const bool tail = VARLEN && (j + 1) * kTile > len;
-    const int win = a.window;
-    const int dmin = CAUSAL ? 0 : (win >= 0 ? -win : INT_MIN);
-    const int dmax = win >= 0 ? win : INT_MAX;
-    QCursor cur{qh0, i_lo};
-    for (int it = 0; it < nq && ok; ++it, q_next(cur)) {
-      const int i = cur.i;
-      const int stage = it & 1;
-      const uint32_t sp = (uint32_t)((it >> 1) & 1);
-      const uint32_t par = (uint32_t)(it & 1);
-      ok = wait_bar_warp(&bars->q_full[stage], sp, wc, kWBwdCmpQ);
-      if (!ok) break;
-      // -LSE_i log2(e) and D_i of this Q tile's rows, in smem after Q_i
-      const float* nlse2 = reinterpret_cast<const float*>(
-          smem + L::kQOff + stage * L::kQStageBytes + L::kTileBytes);
-      const float* dd = nlse2 + kTile;
-      ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
-      if (!ok) break;
-      tc_fence_after();
-      // P^T = exp2(S^T c + LSE2) (LSE2 = -LSE log2 e; packed pairs), in two
-      // halves of 64 queries so that only
-      // half a row of S is live; P half h goes to TMEM columns [32h, 32h+32),
-      // over S columns that have already been read.
-      uint32_t pk[64];
-      const int off0 = (i - j) * kTile;  // q - k where local q = local k
-      const bool edge = tail ||
-                        (dmin != INT_MIN && off0 - (kTile - 1) < dmin) ||
-                        (dmax != INT_MAX && off0 + (kTile - 1) > dmax);
-      // Local query index q is visible to key row r when q_lo <= q <= q_hi.
-      int q_lo = 0, q_hi = kTile - 1;
-      if (edge) {
-        const long long base = off0 - r;  // q - k = base + local q
-        if (dmin != INT_MIN)
-          q_lo = (int)max(0ll, min((long long)kTile, dmin - base));
-        if (dmax != INT_MAX)
-          q_hi = (int)max(-1ll, min((long long)kTile - 1, dmax - base));
-        if (VARLEN && !key_in) q_lo = kTile;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t s[64];
-        tmem_ld32(tl + 64 * h, s);
-        tmem_ld32(tl + 64 * h + 32, s + 32);
-        tmem_wait_ld();
-        reg_fence32(s);
-        reg_fence32(s + 32);
-#pragma unroll
-        for (int e = 0; e < 64; e += 4) {
-          const int q = 64 * h + e;
-          const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + q);
-          float x0, x1, x2, x3;
-          fma2_bc(x0, x1, __uint_as_float(s[e + 0]), __uint_as_float(s[e + 1]),
-                  c2, l4.x, l4.y);
-          fma2_bc(x2, x3, __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]),
-                  c2, l4.z, l4.w);
-          pk[q / 2] = pack_bf16(ex2(x0), ex2(x1));
-          pk[q / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
+    uint32_t g = 0;
+    for (int t = 0; ok; ++t) {
+      int w;
+      ok = sched_take<true>(bars, t, wc, kWBwdCmpSched, w);
+      if (!ok || w >= n_items) break;
+      const BwdItem itm = bwd_item<CAUSAL, VARLEN>(w, n_tiles, a);
+      const int j = itm.j;
+      // Band: query q (global) sees key k when dmin <= q - k <= dmax (INT_MIN
+      // / INT_MAX: no bound); a tile pair needs the mask only if its offsets
+      // reach outside [dmin, dmax].  Tile offsets fit in int because
+      // N <= 2^30 and the window is below N.
+      // With per-sequence lengths, key rows past the sequence's end hold real
+      // (finite) data, so their P must be forced to zero: the tile that holds
+      // the end takes the masked path, with no visible query for those rows.
+      const bool key_in = j * kTile + r < itm.len;
+      const bool tail = VARLEN && (j + 1) * kTile > itm.len;
+      const int win = a.window;
+      const int dmin = CAUSAL ? 0 : (win >= 0 ? -win : INT_MIN);
+      const int dmax = win >= 0 ? win : INT_MAX;
+      QCursor cur{itm.qh0, itm.i_lo};
+      for (int it = 0; it < itm.nq && ok; ++it, q_next(cur, itm)) {
+        const uint32_t gi = g + (uint32_t)it;
+        const int i = cur.i;
+        const int stage = (int)(gi & 1u);
+        const uint32_t sp = (gi >> 1) & 1u;
+        const uint32_t par = gi & 1u;
+        ok = wait_bar_warp(&bars->q_full[stage], sp, wc, kWBwdCmpQ);
+        if (!ok) break;
+        // -LSE_i log2(e) and D_i of this Q tile's rows, in smem after Q_i
+        const float* nlse2 = reinterpret_cast<const float*>(
+            smem + L::kQOff + stage * L::kQStageBytes + L::kTileBytes);
+        const float* dd = nlse2 + kTile;
+        ok = wait_bar_warp(&bars->s_full, par, wc, kWBwdCmpS);
+        if (!ok) break;
+        tc_fence_after();
+        // P^T = exp2(S^T c + LSE2) (LSE2 = -LSE log2 e; packed pairs), in two
+        // halves of 64 queries so that only
+        // half a row of S is live; P half h goes to TMEM columns [32h, 32h+32),
+        // over S columns that have already been read.
+        uint32_t pk[64];
+        const int off0 = (i - j) * kTile;  // q - k where local q = local k
+        const bool edge = tail ||
+                          (dmin != INT_MIN && off0 - (kTile - 1) < dmin) ||
+                          (dmax != INT_MAX && off0 + (kTile - 1) > dmax);
+        // Local query index q is visible to key row r when q_lo <= q <= q_hi.
+        int q_lo = 0, q_hi = kTile - 1;
+        if (edge) {
+          const long long base = off0 - r;  // q - k = base + local q
+          if (dmin != INT_MIN)
+            q_lo = (int)max(0ll, min((long long)kTile, dmin - base));
+          if (dmax != INT_MAX)
+            q_hi = (int)max(-1ll, min((long long)kTile - 1, dmax - base));
+          if (VARLEN && !key_in) q_lo = kTile;
         }
-        if (edge) {  // P of queries outside [q_lo, q_hi] is exactly 0
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int q = 64 * h + 2 * k;
-            uint32_t keep = 0xffffffffu;
-            if (q < q_lo || q > q_hi) keep &= 0xffff0000u;
-            if (q + 1 < q_lo || q + 1 > q_hi) keep &= 0x0000ffffu;
-            pk[32 * h + k] &= keep;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s[64];
+          tmem_ld32(tl + 64 * h, s);
+          tmem_ld32(tl + 64 * h + 32, s + 32);
+          tmem_wait_ld();
+          reg_fence32(s);
+          reg_fence32(s + 32);
+#pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            const int q = 64 * h + e;
+            const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + q);
+            float x0, x1, x2, x3;
+            fma2_bc(x0, x1, __uint_as_float(s[e + 0]), __uint_as_float(s[e + 1]),
+                    c2, l4.x, l4.y);
+            fma2_bc(x2, x3, __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]),
+                    c2, l4.z, l4.w);
+            pk[q / 2] = pack_bf16(ex2(x0), ex2(x1));
+            pk[q / 2 + 1] = pack_bf16(ex2(x2), ex2(x3));
           }
+          if (edge) {  // P of queries outside [q_lo, q_hi] is exactly 0
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int q = 64 * h + 2 * k;
+              uint32_t keep = 0xffffffffu;
+              if (q < q_lo || q > q_hi) keep &= 0xffff0000u;
+              if (q + 1 < q_lo || q + 1 > q_hi) keep &= 0x0000ffffu;
+              pk[32 * h + k] &= keep;
+            }
+          }
+          tmem_st32(tl + 32 * h, pk + 32 * h);
         }
-        tmem_st32(tl + 32 * h, pk + 32 * h);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      warp_arrive(&bars->p_full);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&bars->p_full);
 
-      ok = wait_bar_warp(&bars->dp_full, par, wc, kWBwdCmpDp);
-      if (ok && it > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
+        ok = wait_bar_warp(&bars->dp_full, par, wc, kWBwdCmpDp);
+        if (ok && gi > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
+        if (!ok) break;
+        tc_fence_after();
+        // dS^T goes to smem (read MN-major as dS by the dQ MMA) and, packed to
+        // bf16 pairs, into TMEM columns [128, 192) over dP^T values already
+        // read (the dK MMA takes it from there as its A operand): chunk ch
+        // (32 queries) fills columns 128 + 16 ch .. 128 + 16 ch + 15, which
+        // held dP^T of chunk ch / 2, already loaded.
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t dp[32];
+          tmem_ld32(tl + 128 + ch * 32, dp);
+          tmem_wait_ld();
+          reg_fence32(dp);
+          uint32_t dsk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const int q = ch * 32 + e;
+            const float4 d4 = *reinterpret_cast<const float4*>(dd + q);
+            const uint32_t pa = pk[q / 2], pb = pk[q / 2 + 1];
+            float ds0, ds1, ds2, ds3;
+            mulsub2(ds0, ds1, bf16_lo(pa), bf16_hi(pa), __uint_as_float(dp[e + 0]),
+                    __uint_as_float(dp[e + 1]), d4.x, d4.y);
+            mulsub2(ds2, ds3, bf16_lo(pb), bf16_hi(pb), __uint_as_float(dp[e + 2]),
+                    __uint_as_float(dp[e + 3]), d4.z, d4.w);
+            dsk[e / 2] = pack_bf16(ds0, ds1);
+            dsk[e / 2 + 1] = pack_bf16(ds2, ds3);
+          }
+          // Row r of dS^T, queries ch*32 .. ch*32+31, into the swizzled tile.
+          uint8_t* sub = ds_s + (ch >> 1) * kSubTileBytes;
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint32_t col = (uint32_t)((ch & 1) * 32 + gq * 8);
+            *reinterpret_cast<uint4*>(sub + sw128_offset((uint32_t)r, col)) =
+                make_uint4(dsk[4 * gq], dsk[4 * gq + 1], dsk[4 * gq + 2],
+                           dsk[4 * gq + 3]);
+          }
+          tmem_st16(tl + 128 + ch * 16, dsk);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(&bars->ds_full);
+      }
+      if (!ok) break;
+      // dK epilogue (rows = keys), then the columns are free for the next item
+      ok = wait_bar_warp(&bars->acc_done, (uint32_t)t & 1u, wc, kWBwdCmpAcc);
       if (!ok) break;
       tc_fence_after();
-      // dS^T goes to smem (read MN-major as dS by the dQ MMA) and, packed to
-      // bf16 pairs, into TMEM columns [128, 192) over dP^T values already
-      // read (the dK MMA takes it from there as its A operand): chunk ch
-      // (32 queries) fills columns 128 + 16 ch .. 128 + 16 ch + 15, which
-      // held dP^T of chunk ch / 2, already loaded.
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t dp[32];
-        tmem_ld32(tl + 128 + ch * 32, dp);
-        tmem_wait_ld();
-        reg_fence32(dp);
-        uint32_t dsk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int q = ch * 32 + e;
-          const float4 d4 = *reinterpret_cast<const float4*>(dd + q);
-          const uint32_t pa = pk[q / 2], pb = pk[q / 2 + 1];
-          float ds0, ds1, ds2, ds3;
-          mulsub2(ds0, ds1, bf16_lo(pa), bf16_hi(pa), __uint_as_float(dp[e + 0]),
-                  __uint_as_float(dp[e + 1]), d4.x, d4.y);
-          mulsub2(ds2, ds3, bf16_lo(pb), bf16_hi(pb), __uint_as_float(dp[e + 2]),
-                  __uint_as_float(dp[e + 3]), d4.z, d4.w);
-          dsk[e / 2] = pack_bf16(ds0, ds1);
-          dsk[e / 2 + 1] = pack_bf16(ds2, ds3);
-        }
-        // Row r of dS^T, queries ch*32 .. ch*32+31, into the swizzled tile.
-        uint8_t* sub = ds_s + (ch >> 1) * kSubTileBytes;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t col = (uint32_t)((ch & 1) * 32 + g * 8);
-          *reinterpret_cast<uint4*>(sub + sw128_offset((uint32_t)r, col)) =
-              make_uint4(dsk[4 * g], dsk[4 * g + 1], dsk[4 * g + 2],
-                         dsk[4 * g + 3]);
-        }
-        tmem_st16(tl + 128 + ch * 16, dsk);
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
+      kv_epilogue<D>(tl + 256, a.dk, a.nsplit > 1 ? a.dk_acc : nullptr, itm.bkv,
+                     j * kTile + r, a.N, itm.len, a.scale);
       tc_fence_before();
-      warp_arrive(&bars->ds_full);
-    }
-    // dK epilogue (rows = keys)
-    if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdCmpAcc);
-    if (ok) {
-      tc_fence_after();
-      kv_epilogue<D>(tl + 256, a.dk, a.nsplit > 1 ? a.dk_acc : nullptr, bkv,
-                     j * kTile + r, a.N, len, a.scale);
+      warp_arrive(&bars->acc_free);
+      g += (uint32_t)itm.nq;
     }
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
@@ -579,51 +708,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* const stg_w = stg_s + quarter * 2 * L::kStgBoxBytes;
     constexpr int kBoxes = D / 32;
-    int g = 0;                                       // boxes staged so far
+    int gb = 0;                                      // boxes staged so far
     bool ok = run;
-    QCursor cur{qh0, i_lo};
-    for (int it = 0; it < nq && ok; ++it, q_next(cur)) {
-      const int i = cur.i, bh = cur.bh;
-      ok = wait_bar_warp(&bars->dq_full, (uint32_t)(it & 1), wc, kWBwdDqFull);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t acc[D];
+    uint32_t g = 0;
+    for (int t = 0; ok; ++t) {
+      int w;
+      ok = sched_take<true>(bars, t, wc, kWBwdDqSched, w);
+      if (!ok || w >= n_items) break;
+      const BwdItem itm = bwd_item<CAUSAL, VARLEN>(w, n_tiles, a);
+      QCursor cur{itm.qh0, itm.i_lo};
+      for (int it = 0; it < itm.nq && ok; ++it, q_next(cur, itm)) {
+        const uint32_t gi = g + (uint32_t)it;
+        const int i = cur.i, bh = cur.bh;
+        ok = wait_bar_warp(&bars->dq_full, gi & 1u, wc, kWBwdDqFull);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t acc[D];
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tl + 128 + ch * 32, acc + ch * 32);
-      tmem_wait_ld();
+        for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tl + 128 + ch * 32, acc + ch * 32);
+        tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) reg_fence32(acc + ch * 32);
-      tc_fence_before();
-      warp_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
+        for (int ch = 0; ch < D / 32; ++ch) reg_fence32(acc + ch * 32);
+        tc_fence_before();
+        warp_arrive(&bars->dq_free);   // the dP/dQ columns may be reused now
 #pragma unroll
-      for (int b = 0; b < kBoxes; ++b, ++g) {
-        uint8_t* const buf = stg_w + (g & 1) * L::kStgBoxBytes;
-        if (g >= 2) {
-          if (lane == 0) bulk_wait_read_allbut1();  // box g-2 has been read
+        for (int b = 0; b < kBoxes; ++b, ++gb) {
+          uint8_t* const buf = stg_w + (gb & 1) * L::kStgBoxBytes;
+          if (gb >= 2) {
+            if (lane == 0) bulk_wait_read_allbut1();  // box gb-2 has been read
+            __syncwarp();
+          }
+          uint8_t* dst = buf + lane * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(dst + ((k ^ (lane & 7)) * 16)) =
+                make_uint4(acc[32 * b + 4 * k], acc[32 * b + 4 * k + 1],
+                           acc[32 * b + 4 * k + 2], acc[32 * b + 4 * k + 3]);
+          fence_proxy_async_smem();
           __syncwarp();
-        }
-        uint8_t* dst = buf + lane * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(dst + ((k ^ (lane & 7)) * 16)) =
-              make_uint4(acc[32 * b + 4 * k], acc[32 * b + 4 * k + 1],
-                         acc[32 * b + 4 * k + 2], acc[32 * b + 4 * k + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&tm_dq, buf, b * 32, i * kTile + quarter * 32, bh);
-          bulk_commit_group();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dq, buf, b * 32, i * kTile + quarter * 32, bh);
+            bulk_commit_group();
+          }
         }
       }
-    }
-    if (lane == 0) bulk_wait_all();  // accumulator adds complete before exit
-    // dV epilogue (rows = keys)
-    if (ok) ok = wait_bar_warp(&bars->acc_done, 0, wc, kWBwdDqAcc);
-    if (ok) {
+      if (!ok) break;
+      // dV epilogue (rows = keys), then the columns are free for the next item
+      ok = wait_bar_warp(&bars->acc_done, (uint32_t)t & 1u, wc, kWBwdDqAcc);
+      if (!ok) break;
       tc_fence_after();
       kv_epilogue<D>(tl + 256 + D, a.dv, a.nsplit > 1 ? a.dv_acc : nullptr,
-                     bkv, j * kTile + r, a.N, len, 1.0f);
+                     itm.bkv, itm.j * kTile + r, a.N, itm.len, 1.0f);
+      tc_fence_before();
+      warp_arrive(&bars->acc_free);
+      g += (uint32_t)itm.nq;
     }
+    if (lane == 0) bulk_wait_all();  // accumulator adds complete before exit
   }
 
   tc_fence_before();
@@ -681,6 +821,8 @@ __device__ __forceinline__ void zero_real_rows(float* acc_f, long long heads_tot
 // dK and dV accumulators.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  // The main kernel's work counter starts from zero on every call.
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.work_next = 0u;
   constexpr int kRows = 4;
   constexpr int kPer = D / 32;  // 4 (d=128) or 2 (d=64) elements per lane
   const int lane = threadIdx.x & 31;
@@ -825,15 +967,16 @@ template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdq, const BwdArgs& a,
-                          cudaStream_t stream) {
+                          int grid_blocks, cudaStream_t stream) {
   using L = BwdLayout<D>;
   auto kern = bwd_main_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  dim3 grid((unsigned)(a.BHkv * a.nsplit * n_tiles));
-  kern<<<grid, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  const long long n_items = (long long)a.BHkv * a.nsplit * n_tiles;
+  const int blocks = n_items < grid_blocks ? (int)n_items : grid_blocks;
+  kern<<<blocks, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -851,20 +994,21 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdq, const BwdArgs& a, int d,
-                            bool causal, cudaStream_t stream) {
+                            bool causal, int grid_blocks, cudaStream_t stream) {
   const bool vl = a.seq_lens != nullptr;
+  const int gb = grid_blocks;
   if (d == 128) {
     if (causal)
-      return vl ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tdq, a, stream)
-                : launch_main_t<128, true, false>(tq, tk, tv, tdo, tdq, a, stream);
-    return vl ? launch_main_t<128, false, true>(tq, tk, tv, tdo, tdq, a, stream)
-              : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdq, a, stream);
+      return vl ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
+                : launch_main_t<128, true, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
+    return vl ? launch_main_t<128, false, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
+              : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
   }
   if (causal)
-    return vl ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tdq, a, stream)
-              : launch_main_t<64, true, false>(tq, tk, tv, tdo, tdq, a, stream);
-  return vl ? launch_main_t<64, false, true>(tq, tk, tv, tdo, tdq, a, stream)
-            : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdq, a, stream);
+    return vl ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
+              : launch_main_t<64, true, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
+  return vl ? launch_main_t<64, false, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
+            : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
 }
 
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,

@@ -60,6 +60,7 @@ struct BwdArgs {
   int group;                  // key/value heads per scheduling group
   float scale;
   float scale_log2;
+  unsigned int* work_next;    // main kernel's work counter (workspace)
   DevState* st;
   uint64_t timeout_ns;
 };
@@ -80,10 +81,11 @@ cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
                               int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
                            cudaStream_t stream);
+// Persistent: min(work items, grid_blocks) blocks, one per SM.
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdq, const BwdArgs& a, int d,
-                            bool causal, cudaStream_t stream);
+                            bool causal, int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
                             cudaStream_t stream);
 cudaError_t launch_expire_wait(DevState* st, uint64_t timeout_ns,
