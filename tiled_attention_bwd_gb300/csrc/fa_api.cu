@@ -19,6 +19,12 @@
 namespace {
 
 __device__ fa::DevState g_dev_state;  // zero-initialised at module load
+// Work counters of forward calls: (next item, finished blocks) per slot,
+// zero-initialised; each call takes the next slot and its last block sets
+// the pair back to zero.  Calls more than kFwdSchedSlots apart may reuse a
+// slot only after the earlier one has finished.
+constexpr unsigned kFwdSchedSlots = 64;
+__device__ unsigned int g_fwd_sched[kFwdSchedSlots][2];
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
@@ -29,6 +35,8 @@ constexpr int kMaxN = 1 << 30;  // keeps every row index inside int
 struct DeviceCtx {
   bool ready = false;
   fa::DevState* state = nullptr;
+  unsigned int* fwd_sched = nullptr;  // device address of g_fwd_sched
+  std::atomic<unsigned> fwd_slot{0};
   int sm_count = 0;
 };
 DeviceCtx g_ctx[kMaxDevices];
@@ -54,12 +62,42 @@ fa_status device_ctx(DeviceCtx** out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
         cudaSuccess)
       return FA_ERR_CUDA;
+    void* ps = nullptr;
+    if (cudaGetSymbolAddress(&ps, g_fwd_sched) != cudaSuccess) return FA_ERR_CUDA;
     c.state = static_cast<fa::DevState*>(p);
+    c.fwd_sched = static_cast<unsigned int*>(ps);
     c.sm_count = sms;
     c.ready = true;
   }
   *out = &c;
   return FA_OK;
+}
+
+// The work counter slot of one forward call.
+void fwd_sched_slot(DeviceCtx* ctx, fa::FwdArgs& a) {
+  const unsigned slot = ctx->fwd_slot.fetch_add(1u) % kFwdSchedSlots;
+  a.work_next = ctx->fwd_sched + 2 * slot;
+  a.work_done = a.work_next + 1;
+}
+
+// Schedule of the forward.  When every head's K and V (4 d bytes per row
+// and head) fit in L2 together, one group of all heads, dealt in alternating
+// rounds (measured best there: the last items are the lightest of all).
+// Otherwise groups of as many heads as keep their K and V within a share of
+// L2, with items claimed dynamically so that the groups cost no balance.
+void fwd_schedule(int BH, int N, int d, fa::FwdArgs& a) {
+  constexpr size_t kAll = 96u << 20, kBudget = 48u << 20;
+  const size_t per_head = (size_t)4 * N * d;
+  if (per_head * (size_t)BH <= kAll) {
+    a.group = BH;
+    a.dynamic = 0;
+    return;
+  }
+  size_t g = per_head ? kBudget / per_head : (size_t)BH;
+  if (g < 1) g = 1;
+  if (g > (size_t)BH) g = (size_t)BH;
+  a.group = (int)g;
+  a.dynamic = 1;
 }
 
 fa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
@@ -290,10 +328,11 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   // of N - 1 hides no key, so a call with lengths and no window runs there.
   a.window = (seq_lens && win < 0) ? N - 1 : win;
   a.seq_lens = seq_lens;
-  a.group = BH;  // the forward schedules over all heads at once
+  fwd_schedule(BH, N, d, a);
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = g_timeout_ns.load();
+  fwd_sched_slot(ctx, a);
   cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
                                  ctx->sm_count, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -522,13 +561,14 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.H = H;
   a.Hkv = H;
   a.window = -1;
-  a.group = BH;
+  fwd_schedule(BH, N, d, a);
   a.scale_log2 = scale * fa::kLog2e;
   a.q_scale = sq;
   a.k_scale = sk;
   a.n_sblk = nsb;
   a.st = ctx->state;
   a.timeout_ns = g_timeout_ns.load();
+  fwd_sched_slot(ctx, a);
   e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, causal != 0, ctx->sm_count, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -90,6 +90,9 @@ struct FwdBars {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t mma_done;
+  uint64_t sched_full[2];   // work item t published in sched_item[t % 2]
+  uint64_t sched_empty[2];  // ... and read by the MMA thread and 8 warps
+  int sched_item[2];
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -98,6 +101,9 @@ struct FwdBars {
 enum : uint32_t {
   kWFwdProdEmpty = 0x101,
   kWFwdProdQ = 0x102,
+  kWFwdProdSched = 0x103,
+  kWFwdMmaSched = 0x204,
+  kWFwdSmSched = 0x303,
   kWFwdMmaQ = 0x201,
   kWFwdMmaKV = 0x202,
   kWFwdMmaP = 0x203,
@@ -173,10 +179,9 @@ struct FwdItem {
   int bh, kvh, qt0, qt1, lo0, hi0, lo1, hi1, jb, je;
   int len;  // rows of this batch entry's sequence (N without lengths)
 };
-// Items are ordered heaviest first over the whole grid (pair index slow,
-// head fast; causal pairs from the last one down).  Measured: grouping heads
-// so that their K/V stay in L2 cut DRAM reads but cost more in balance than
-// it saved, so the forward uses the global order.
+// Items come in groups of heads whose K and V fit in L2 together, heaviest
+// first within a group (pair index slow, head fast; causal pairs from the
+// last one down).
 // Balanced item order with per-sequence lengths.  The plain order assumes
 // that every head has the same items; with lengths, items past a sequence's
 // end are empty and the dealing of the remaining ones to blocks loses its
@@ -322,9 +327,16 @@ __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
   if (VARLEN && tab) {
     table_item<CAUSAL>(w, tab, a.BH / a.H, a.H, n_pairs, it.bh, pair);
   } else {
-    const int rank = w / a.BH;
+    // Groups of a.group heads whose K and V fit in L2 together; within a
+    // group the pair index is slow (heaviest first) and the head fast.
+    const int per_group = a.group * n_pairs;
+    const int grp = w / per_group;
+    const int rr = w - grp * per_group;
+    const int rest = a.BH - grp * a.group;
+    const int heads = rest < a.group ? rest : a.group;
+    const int rank = rr / heads;
     pair = CAUSAL ? (n_pairs - 1 - rank) : rank;
-    it.bh = w - rank * a.BH;
+    it.bh = grp * a.group + (rr - rank * heads);
   }
   const int b = it.bh / a.H, h = it.bh - b * a.H;
   it.kvh = b * a.Hkv + h / (a.H / a.Hkv);
@@ -351,15 +363,44 @@ __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
   return it;
 }
 
-// Item of block b in round r: rounds of gridDim.x items are dealt to the
-// blocks alternately forwards and backwards, so that with items sorted by
-// decreasing cost every block gets a similar total.
+// Work items are handed out in one of two ways.  When every head's K and V
+// fit in L2 together, in rounds of gridDim.x items dealt to the blocks
+// alternately forwards and backwards, so that with items sorted by
+// decreasing cost every block gets a similar total.  Otherwise dynamically
+// (a.dynamic): block b starts with item b and then claims the next
+// unclaimed one from a counter in device memory, so that the head groups
+// cost no balance.  The counter belongs to this call (a slot of a ring the
+// host hands out); the last block to finish sets it back to zero for the
+// slot's next call.  Either way the producer thread publishes each item in
+// a two-slot ring in shared memory, which the MMA thread and the softmax
+// warps read in the same order.
 __device__ __forceinline__ int fwd_round_item(int r) {
   const int g = (int)gridDim.x, b = (int)blockIdx.x;
   return r * g + ((r & 1) ? (g - 1 - b) : b);
 }
 
-// Persistent: one block per SM walks its items round by round.  Barrier
+// Item t of this block: the alternating rounds, computed locally, or (with
+// a.dynamic) the one the producer published.
+template <int S>
+__device__ __forceinline__ bool fwd_take(FwdBars<S>* bars, int t, bool warp_wide,
+                                         const FwdArgs& a, const WaitCtl& wc,
+                                         uint32_t where, int& w) {
+  if (!a.dynamic) {
+    w = fwd_round_item(t);
+    return true;
+  }
+  const int sl = t & 1;
+  const uint32_t par = (uint32_t)(t >> 1) & 1u;
+  bool ok = wait_bar<true>(&bars->sched_full[sl], par, wc, where);
+  if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  w = *reinterpret_cast<volatile int*>(&bars->sched_item[sl]);
+  if (warp_wide) warp_arrive(&bars->sched_empty[sl]);
+  else mbar_arrive(&bars->sched_empty[sl]);
+  return true;
+}
+
+// Persistent: one block per SM takes items one after another.  Barrier
 // phases run on across items, so the producer fetches the next item's Q and
 // K/V while the current one finishes, and the next item's first Q K^T
 // overlaps the softmax warps' epilogue.
@@ -407,6 +448,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars->kv_empty[s], 1);
     }
     mbar_init(&bars->mma_done, 1);
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(&bars->sched_full[sl], 1);
+      mbar_init(&bars->sched_empty[sl], 9);  // MMA thread + 8 softmax warps
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -436,10 +481,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t phase = 0;
       uint32_t q_cnt0 = 0, q_cnt1 = 0;   // loads issued into each Q buffer
       bool ok = true;
-      for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
-           w = fwd_round_item(++r)) {
-        const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
-        if (VARLEN && itm.hi0 < 0) continue;  // empty (past its sequence's end)
+      for (int ti = 0; ok; ++ti) {
+        FwdItem itm;
+        int w;
+        if (!a.dynamic) {
+          // Alternating rounds: every role computes the same sequence.
+          w = fwd_round_item(ti);
+          if (w >= n_items) break;
+          itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
+          if (VARLEN && itm.hi0 < 0) continue;  // empty (past its sequence's end)
+        } else {
+          // Claim the next item with work (with per-sequence lengths some
+          // are empty) and publish it; n_items or more tells the others to
+          // stop.
+          w = ti > 0 ? (int)gridDim.x + (int)atomicAdd(a.work_next, 1u)
+                     : (int)blockIdx.x;
+          while (w < n_items) {
+            itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
+            if (!VARLEN || itm.hi0 >= 0) break;
+            w = (int)gridDim.x + (int)atomicAdd(a.work_next, 1u);
+          }
+          ok = wait_bar<kInl>(&bars->sched_empty[ti & 1],
+                              ((uint32_t)(ti >> 1) & 1u) ^ 1u, wc, kWFwdProdSched);
+          if (!ok) break;
+          *reinterpret_cast<volatile int*>(&bars->sched_item[ti & 1]) = w;
+          mbar_arrive(&bars->sched_full[ti & 1]);
+          if (w >= n_items) break;
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || (t == 1 && itm.hi1 < 0)) break;
@@ -524,10 +592,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(&bars->s_full[t]);
         if (x == hi_t) mma_commit(&bars->q_empty[t]);
       };
-      for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
-           w = fwd_round_item(++r)) {
+      for (int ti = 0; ok; ++ti) {
+        int w;
+        ok = fwd_take(bars, ti, false, a, wc, kWFwdMmaSched, w);
+        if (!ok || w >= n_items) break;
         const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
-        if (VARLEN && itm.hi0 < 0) continue;  // empty item
+        if (VARLEN && itm.hi0 < 0) continue;  // empty item (alternating rounds)
         auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
         auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
         ok = wait_bar<kInl>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
@@ -597,8 +667,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float c = a.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = run;
-    for (int r = 0, w = fwd_round_item(0); w < n_items && ok;
-         w = fwd_round_item(++r)) {
+    for (int ti = 0; ok; ++ti) {
+      int w;
+      ok = fwd_take(bars, ti, true, a, wc, kWFwdSmSched, w);
+      if (!ok || w >= n_items) break;
       const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
       const int lo_t = t ? itm.lo1 : itm.lo0;
       const int hi_t = t ? itm.hi1 : itm.hi0;
@@ -794,6 +866,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  // Every block has stopped claiming; the last one out resets the counter.
+  if (a.dynamic && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.work_done, 1u) == gridDim.x - 1) {
+      atomicExch(a.work_next, 0u);
+      atomicExch(a.work_done, 0u);
+    }
   }
 }
 

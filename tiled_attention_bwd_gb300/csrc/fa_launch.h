@@ -31,6 +31,12 @@ struct FwdArgs {
   const float* q_scale;
   const float* k_scale;
   int n_sblk;
+  // 1: blocks claim items from this call's work counter (a slot of a
+  // zero-initialised ring, with its count of finished blocks; the last
+  // block resets both); 0: items are dealt in alternating rounds.
+  int dynamic;
+  unsigned int* work_next;
+  unsigned int* work_done;
   DevState* st;
   uint64_t timeout_ns;
 };
