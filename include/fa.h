@@ -256,11 +256,48 @@ fa_status fa_check_device_status(void* stream);
 /*
  * Time limit, in nanoseconds, of every pipeline wait inside the kernels
  * launched after this call (default 2e9 = 2 s).  A wait that runs past it
- * records FA_ERR_DEVICE_TIMEOUT, stops its thread block cleanly (in-flight
- * copies drained, tensor memory released) and makes the other blocks of the
- * grid stop at their next wait.  Values of 0 restore the default.
+ * records FA_ERR_DEVICE_TIMEOUT,
+ * stops its thread block cleanly (in-flight copies drained, tensor memory
+ * released) and makes the other blocks of the grid stop at their next wait.
+ * Values of 0 restore the default.
  */
 void fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook of the failure path, for the current device.  Until called
+ * again with 0, every pipeline wait at `site` inside the forward and
+ * backward kernels launched after this call that finds its barrier not yet
+ * complete (a real wait) behaves as if its time limit had passed: it
+ * records FA_ERR_DEVICE_TIMEOUT with that
+ * site, and its block and the rest of the grid stop exactly as after a real
+ * timeout (nothing is faulted, trapped or left hanging).  A site is a
+ * where-code, role * 256 + n:
+ *   forward:  0x101 producer waiting for a K/V ring slot, 0x102 producer
+ *             waiting for a Q buffer, 0x103 producer waiting to publish a
+ *             claimed item; 0x201 MMA thread waiting for Q, 0x202 for K/V,
+ *             0x203 for P, 0x204 for the next item; 0x301 softmax waiting
+ *             for S, 0x302 for the finished O, 0x303 for the next item.
+ *   backward: 0x111 producer waiting for a Q stage, 0x112 for the dO
+ *             buffer, 0x113 for the K buffer, 0x114 for the V buffer, 0x115
+ *             to publish an item; 0x211 MMA thread waiting for K/V, 0x212
+ *             Q, 0x213 the dQ read-out, 0x214 P, 0x215 dS, 0x216 dO, 0x217
+ *             the dK/dV read-out, 0x218 the next item; 0x311 P/dS warps
+ *             waiting for Q, 0x312 S, 0x313 dP, 0x314 the dS buffer, 0x315
+ *             the finished dK, 0x316 the next item; 0x411 dQ drain waiting
+ *             for dQ, 0x412 the finished dV, 0x413 the next item.
+ * The call is synchronous (it writes a constant in device memory): make it
+ * only while no kernel of this library is running on the device.
+ * The pages have no counterpart; this exists so that the failure handling
+ * of the real kernels can be tested without harming the GPU.
+ */
+void fa_debug_expire_at(uint32_t site);
+
+/*
+ * Site (where-code, as listed at fa_debug_expire_at) of the failure that the
+ * last fa_check_device_status call of the calling thread reported; 0 if that
+ * call reported none.
+ */
+uint32_t fa_last_failure_site(void);
 
 /*
  * Launches one small kernel whose thread waits, with the configured time

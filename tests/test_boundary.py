@@ -30,7 +30,8 @@ def test_header_declares_the_expected_entry_points():
               "fa_fwd_varlen", "fa_bwd_varlen",
               "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_quantize_e4m3",
               "fa_check_device_status", "fa_status_string",
-              "fa_set_wait_timeout_ns", "fa_debug_expire_wait"):
+              "fa_set_wait_timeout_ns", "fa_debug_expire_wait",
+              "fa_debug_expire_at", "fa_last_failure_site"):
         assert n in names
 
 

@@ -29,6 +29,8 @@ __device__ unsigned int g_fwd_sched[kFwdSchedSlots][2];
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 
+uint64_t kernel_timeout() { return g_timeout_ns.load(); }
+
 constexpr int kMaxDevices = 64;
 constexpr int kMaxN = 1 << 30;  // keeps every row index inside int
 
@@ -42,6 +44,7 @@ struct DeviceCtx {
 DeviceCtx g_ctx[kMaxDevices];
 std::mutex g_ctx_mu;
 
+thread_local uint32_t g_last_where = 0;  // site of the last reported failure
 thread_local cudaEvent_t g_ev_before_main = nullptr;
 thread_local cudaEvent_t g_ev_after_main = nullptr;
 
@@ -289,6 +292,11 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
+void fa_debug_expire_at(uint32_t site) {
+  (void)fa::set_expire_site_fwd(site);
+  (void)fa::set_expire_site_bwd(site);
+}
+
 void fa_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
 }
@@ -331,7 +339,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   fwd_schedule(BH, N, d, a);
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
-  a.timeout_ns = g_timeout_ns.load();
+  a.timeout_ns = kernel_timeout();
   fwd_sched_slot(ctx, a);
   cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
                                  ctx->sm_count, static_cast<cudaStream_t>(stream));
@@ -443,7 +451,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   a.scale = scale;
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
-  a.timeout_ns = g_timeout_ns.load();
+  a.timeout_ns = kernel_timeout();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int elem_blocks = ctx->sm_count * 8;
   cudaError_t e = fa::launch_bwd_pre(a, d, elem_blocks, st);
@@ -567,7 +575,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.k_scale = sk;
   a.n_sblk = nsb;
   a.st = ctx->state;
-  a.timeout_ns = g_timeout_ns.load();
+  a.timeout_ns = kernel_timeout();
   fwd_sched_slot(ctx, a);
   e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, causal != 0, ctx->sm_count, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -588,7 +596,9 @@ fa_status fa_check_device_status(void* stream) {
   if (cudaMemcpy(&h, ctx->state, sizeof(h), cudaMemcpyDeviceToHost) !=
       cudaSuccess)
     return FA_ERR_CUDA;
+  g_last_where = 0;
   if (h.status == 0 && h.abort == 0) return FA_OK;
+  g_last_where = h.where;
   if (cudaMemset(ctx->state, 0, sizeof(fa::DevState)) != cudaSuccess)
     return FA_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
@@ -596,11 +606,13 @@ fa_status fa_check_device_status(void* stream) {
                        : FA_ERR_DEVICE_TIMEOUT;
 }
 
+uint32_t fa_last_failure_site(void) { return g_last_where; }
+
 fa_status fa_debug_expire_wait(void* stream) {
   DeviceCtx* ctx = nullptr;
   fa_status s = device_ctx(&ctx);
   if (s != FA_OK) return s;
-  cudaError_t e = fa::launch_expire_wait(ctx->state, g_timeout_ns.load(),
+  cudaError_t e = fa::launch_expire_wait(ctx->state, kernel_timeout(),
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -1017,4 +1017,8 @@ cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
   return cudaGetLastError();
 }
 
+cudaError_t set_expire_site_bwd(uint32_t site) {
+  return cudaMemcpyToSymbol(c_expire_site, &site, sizeof(site));
+}
+
 }  // namespace fa

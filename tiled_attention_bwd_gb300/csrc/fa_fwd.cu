@@ -1032,4 +1032,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                 : launch_fwd_w<64, false>(tq, tk, tv, a, BH, grid_blocks, stream);
 }
 
+cudaError_t set_expire_site_fwd(uint32_t site) {
+  return cudaMemcpyToSymbol(c_expire_site, &site, sizeof(site));
+}
+
 }  // namespace fa

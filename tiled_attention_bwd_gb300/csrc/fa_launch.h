@@ -96,5 +96,10 @@ cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
                             cudaStream_t stream);
 cudaError_t launch_expire_wait(DevState* st, uint64_t timeout_ns,
                                cudaStream_t stream);
+// The failure-path test hook of the forward / backward kernels (the site
+// whose waits expire at once, 0 for none), for the current device.
+// Synchronous; call only while no kernel of the library runs.
+cudaError_t set_expire_site_fwd(uint32_t site);
+cudaError_t set_expire_site_bwd(uint32_t site);
 
 }  // namespace fa

@@ -7,7 +7,8 @@ the library has not been built, loading it raises immediately.
 
 Names mirror the C ABI: ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``,
 ``fa_check_device_status``, ``fa_set_wait_timeout_ns``,
-``fa_debug_expire_wait``, ``fa_bwd_set_phase_events``, ``fa_status_string``.
+``fa_debug_expire_wait``, ``fa_debug_expire_at``, ``fa_last_failure_site``,
+``fa_bwd_set_phase_events``, ``fa_status_string``.
 """
 import ctypes
 import os
@@ -92,6 +93,10 @@ def open_library(path: str):
     lib.fa_set_wait_timeout_ns.restype = None
     lib.fa_debug_expire_wait.argtypes = [vp]
     lib.fa_debug_expire_wait.restype = i
+    lib.fa_debug_expire_at.argtypes = [ctypes.c_uint32]
+    lib.fa_debug_expire_at.restype = None
+    lib.fa_last_failure_site.argtypes = []
+    lib.fa_last_failure_site.restype = ctypes.c_uint32
     lib.fa_bwd_set_phase_events.argtypes = [vp, vp]
     lib.fa_bwd_set_phase_events.restype = None
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -162,6 +167,18 @@ def fa_check_device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the status code."""
     dev = torch.device("cuda") if device is None else torch.device(device)
     return int(load_library().fa_check_device_status(_stream_handle(dev)))
+
+
+def fa_debug_expire_at(site: int) -> None:
+    """Make every pipeline wait at `site` (a where-code, see include/fa.h) in
+    later launches behave as if its time limit had passed; 0 turns it off."""
+    load_library().fa_debug_expire_at(int(site))
+
+
+def fa_last_failure_site() -> int:
+    """Where-code of the failure the last fa_check_device_status call on this
+    thread reported (0: none)."""
+    return int(load_library().fa_last_failure_site())
 
 
 def fa_debug_expire_wait(device=None) -> None:
