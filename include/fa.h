@@ -285,8 +285,13 @@ void fa_set_wait_timeout_ns(uint64_t ns);
  *             waiting for Q, 0x312 S, 0x313 dP, 0x314 the dS buffer, 0x315
  *             the finished dK, 0x316 the next item; 0x411 dQ drain waiting
  *             for dQ, 0x412 the finished dV, 0x413 the next item.
- * The call is synchronous (it writes a constant in device memory): make it
- * only while no kernel of this library is running on the device.
+ * While a site is set, forward and backward calls with d = 128 and no
+ * window, lengths or FP8 run kernel instantiations compiled with the hook
+ * (the same source; the ones used otherwise carry no trace of it, since
+ * even a test on the slow path of each wait cost about 1%); other calls
+ * ignore it.  The call is synchronous (it writes a constant in device
+ * memory): make it only while no kernel of this library is running on the
+ * device.
  * The pages have no counterpart; this exists so that the failure handling
  * of the real kernels can be tested without harming the GPU.
  */

@@ -30,6 +30,9 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 
 uint64_t kernel_timeout() { return g_timeout_ns.load(); }
+// Set while the failure-path test hook has a site: launches then use the
+// instantiations compiled with the hook.
+std::atomic<bool> g_hook_on{false};
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxN = 1 << 30;  // keeps every row index inside int
@@ -84,14 +87,18 @@ void fwd_sched_slot(DeviceCtx* ctx, fa::FwdArgs& a) {
 }
 
 // Schedule of the forward.  When every head's K and V (4 d bytes per row
-// and head) fit in L2 together, one group of all heads, dealt in alternating
-// rounds (measured best there: the last items are the lightest of all).
-// Otherwise groups of as many heads as keep their K and V within a share of
-// L2, with items claimed dynamically so that the groups cost no balance.
+// and head) fit in L2 together, or a window is set (a band's K and V stay in
+// L2 anyway), one group of all heads, dealt in alternating rounds (measured
+// best there: the last items are the lightest of all).  Otherwise groups of
+// as many heads as keep their K and V within a share of L2, with items
+// claimed dynamically (a separate kernel instantiation) so that the groups
+// cost no balance.
 void fwd_schedule(int BH, int N, int d, fa::FwdArgs& a) {
   constexpr size_t kAll = 96u << 20, kBudget = 48u << 20;
   const size_t per_head = (size_t)4 * N * d;
-  if (per_head * (size_t)BH <= kAll) {
+  // (With per-sequence lengths the call always runs with a window, N - 1
+  // at widest, so it takes this branch too.)
+  if (a.window >= 0 || per_head * (size_t)BH <= kAll) {
     a.group = BH;
     a.dynamic = 0;
     return;
@@ -295,6 +302,7 @@ const char* fa_status_string(fa_status s) {
 void fa_debug_expire_at(uint32_t site) {
   (void)fa::set_expire_site_fwd(site);
   (void)fa::set_expire_site_bwd(site);
+  g_hook_on.store(site != 0);
 }
 
 void fa_set_wait_timeout_ns(uint64_t ns) {
@@ -340,6 +348,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = kernel_timeout();
+  a.hook = g_hook_on.load() ? 1 : 0;
   fwd_sched_slot(ctx, a);
   cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
                                  ctx->sm_count, static_cast<cudaStream_t>(stream));
@@ -452,6 +461,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = kernel_timeout();
+  a.hook = g_hook_on.load() ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int elem_blocks = ctx->sm_count * 8;
   cudaError_t e = fa::launch_bwd_pre(a, d, elem_blocks, st);
@@ -576,6 +586,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.n_sblk = nsb;
   a.st = ctx->state;
   a.timeout_ns = kernel_timeout();
+  a.hook = g_hook_on.load() ? 1 : 0;
   fwd_sched_slot(ctx, a);
   e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, causal != 0, ctx->sm_count, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -255,7 +255,7 @@ __device__ __forceinline__ void q_next(QCursor& c, const BwdItem& itm) {
 // dO tiles load while the current one finishes, its K as soon as the last
 // MMA reading K_j is done, and its first S^T / dP^T overlap the read-out of
 // the current dK_j, dV_j.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HOOK>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -346,14 +346,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!VARLEN || itm.nq > 0) break;
           w = (int)gridDim.x + (int)atomicAdd(a.work_next, 1u);
         }
-        ok = wait_bar(&bars->sched_empty[t & 1], ((uint32_t)(t >> 1) & 1u) ^ 1u, wc,
+        ok = wait_bar<false, HOOK>(&bars->sched_empty[t & 1], ((uint32_t)(t >> 1) & 1u) ^ 1u, wc,
                       kWBwdProdSched);
         if (!ok) break;
         *reinterpret_cast<volatile int*>(&bars->sched_item[t & 1]) = w;
         mbar_arrive(&bars->sched_full[t & 1]);
         if (w >= n_items) break;
         // V_j as soon as the previous item's last dP^T has read its V.
-        if (t > 0) ok = wait_bar(&bars->v_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdVEmpty);
+        if (t > 0) ok = wait_bar<false, HOOK>(&bars->v_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdVEmpty);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars->v_full, L::kTileBytes);
 #pragma unroll
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int stage = (int)(g & 1u);
           const uint32_t sp = (g >> 1) & 1u;
           // Q_i, LSE2_i, D_i into Q stage g % 2
-          ok = wait_bar(&bars->q_empty[stage], sp ^ 1u, wc, kWBwdProdQEmpty);
+          ok = wait_bar<false, HOOK>(&bars->q_empty[stage], sp ^ 1u, wc, kWBwdProdQEmpty);
           if (!ok) break;
           uint8_t* qs = smem + L::kQOff + stage * L::kQStageBytes;
           mbar_arrive_expect_tx(&bars->q_full[stage], L::kTileBytes + 2 * kTile * 4);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     &bars->q_full[stage]);
           q_par[stage] = (int)sp;
           // dO_i into the single dO buffer
-          ok = wait_bar(&bars->do_empty, (g & 1u) ^ 1u, wc, kWBwdProdDoEmpty);
+          ok = wait_bar<false, HOOK>(&bars->do_empty, (g & 1u) ^ 1u, wc, kWBwdProdDoEmpty);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars->do_full, L::kTileBytes);
 #pragma unroll
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (it == 0) {
             // K_j once the previous item's last MMA reading K is done (its
             // first Q and dO are already on their way).
-            if (t > 0) ok = wait_bar(&bars->k_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdKEmpty);
+            if (t > 0) ok = wait_bar<false, HOOK>(&bars->k_empty, (uint32_t)(t - 1) & 1u, wc, kWBwdProdKEmpty);
             if (!ok) break;
             mbar_arrive_expect_tx(&bars->k_full, L::kTileBytes);
 #pragma unroll
@@ -469,14 +469,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tp = (uint32_t)t & 1u;
         // The item's first S^T and dP^T.  dP^T(0) reuses the columns of the
         // previous item's last dQ, which the drain warps must have read.
-        ok = wait_bar(&bars->k_full, tp, wc, kWBwdMmaKV);
-        if (ok) ok = wait_bar(&bars->q_full[g & 1u], (g >> 1) & 1u, wc, kWBwdMmaQ);
+        ok = wait_bar<false, HOOK>(&bars->k_full, tp, wc, kWBwdMmaKV);
+        if (ok) ok = wait_bar<false, HOOK>(&bars->q_full[g & 1u], (g >> 1) & 1u, wc, kWBwdMmaQ);
         if (!ok) break;
         tc_fence_after();
         issue_st(g);
-        ok = wait_bar(&bars->v_full, tp, wc, kWBwdMmaKV);
-        if (ok) ok = wait_bar(&bars->do_full, g & 1u, wc, kWBwdMmaDo);
-        if (ok && g > 0) ok = wait_bar(&bars->dq_free, (g - 1u) & 1u, wc, kWBwdMmaDqFree);
+        ok = wait_bar<false, HOOK>(&bars->v_full, tp, wc, kWBwdMmaKV);
+        if (ok) ok = wait_bar<false, HOOK>(&bars->do_full, g & 1u, wc, kWBwdMmaDo);
+        if (ok && g > 0) ok = wait_bar<false, HOOK>(&bars->dq_free, (g - 1u) & 1u, wc, kWBwdMmaDqFree);
         if (!ok) break;
         tc_fence_after();
         issue_dp();
@@ -484,11 +484,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; it < nq && ok; ++it) {
           const uint32_t gi = g + (uint32_t)it;
           const uint32_t par = gi & 1u;
-          ok = wait_bar(&bars->p_full, par, wc, kWBwdMmaP);
+          ok = wait_bar<false, HOOK>(&bars->p_full, par, wc, kWBwdMmaP);
           // dK, dV of the previous item must be out of TMEM before this
           // item's first products overwrite them.
           if (ok && it == 0 && t > 0)
-            ok = wait_bar(&bars->acc_free, tp ^ 1u, wc, kWBwdMmaAccFree);
+            ok = wait_bar<false, HOOK>(&bars->acc_free, tp ^ 1u, wc, kWBwdMmaAccFree);
           if (!ok) break;
           tc_fence_after();
           // dV_j += P^T dO_i   [keys x d], K = queries; P^T from TMEM
@@ -498,13 +498,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    (it > 0 || s > 0) ? 1u : 0u);
           mma_commit(&bars->do_empty);   // dO_i no longer needed
           if (it + 1 < nq) {
-            ok = wait_bar(&bars->q_full[(gi + 1u) & 1u], ((gi + 1u) >> 1) & 1u,
+            ok = wait_bar<false, HOOK>(&bars->q_full[(gi + 1u) & 1u], ((gi + 1u) >> 1) & 1u,
                           wc, kWBwdMmaQ);
             if (!ok) break;
             tc_fence_after();
             issue_st(gi + 1u);
           }
-          ok = wait_bar(&bars->ds_full, par, wc, kWBwdMmaDs);
+          ok = wait_bar<false, HOOK>(&bars->ds_full, par, wc, kWBwdMmaDs);
           if (!ok) break;
           tc_fence_after();
           // dK_j += dS^T Q_i   [keys x d], K = queries; dS^T from TMEM (bf16
@@ -524,8 +524,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(&bars->ds_free);    // dS_i no longer read
           if (it + 1 < nq) {
             // dQ_it occupies the dP columns until the drain warps have read it.
-            ok = wait_bar(&bars->dq_free, par, wc, kWBwdMmaDqFree);
-            if (ok) ok = wait_bar(&bars->do_full, par ^ 1u, wc, kWBwdMmaDo);
+            ok = wait_bar<false, HOOK>(&bars->dq_free, par, wc, kWBwdMmaDqFree);
+            if (ok) ok = wait_bar<false, HOOK>(&bars->do_full, par ^ 1u, wc, kWBwdMmaDo);
             if (!ok) break;
             tc_fence_after();
             issue_dp();
@@ -963,13 +963,20 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HOOK = false>
 cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
                           const CUtensorMap& tdq, const BwdArgs& a,
                           int grid_blocks, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto kern = bwd_main_kernel<D, CAUSAL, VARLEN>;
+  // The failure-path test hook has its own instantiation, for d = 128
+  // without per-sequence lengths only.
+  if constexpr (D == 128 && !VARLEN && !HOOK) {
+    if (a.hook)
+      return launch_main_t<D, CAUSAL, VARLEN, true>(tq, tk, tv, tdo, tdq, a,
+                                                    grid_blocks, stream);
+  }
+  auto kern = bwd_main_kernel<D, CAUSAL, VARLEN, HOOK>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;

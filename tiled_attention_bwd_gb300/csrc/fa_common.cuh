@@ -33,13 +33,14 @@ struct WaitCtl {
   uint64_t timeout_ns;
 };
 
-// Test hook of the failure path: every wait whose where-code equals this
-// value and whose barrier is not complete at its first test behaves as if
-// its time limit had passed (it records the timeout and stops the grid, like
-// a real one); 0 (the default) matches none.  It is read only on that slow
-// path: a test in front of every wait was measured to cost 12% of the
-// backward.  One copy per translation unit, set by the host between
-// launches (set_expire_site_*).
+// Failure-path test hook.  In the kernel instantiations compiled with it
+// (kHook), a wait whose where-code equals c_expire_site and whose barrier
+// is not complete at its first test behaves as if its time limit had
+// passed: it records the timeout and stops the grid like a real one.  The
+// production instantiations carry none of it: even on the slow path alone
+// the test cost about 1% of the backward.  One copy of the site per
+// translation unit, set by the host between launches (set_expire_site_*);
+// 0 (the default) matches none.
 static __constant__ uint32_t c_expire_site;
 
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
@@ -57,23 +58,22 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t where) {
 // Wait for the phase of `bar` with the given parity.  Returns false (and
 // never blocks longer than the time limit) if the wait expired here or the
 // block / grid is already stopping.
+template <bool kHook>
 __device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
                                               const WaitCtl& c, uint32_t where) {
-  if (c_expire_site == where) {  // test hook (a real wait only)
-    raise_abort(c, where);
-    return false;
-  }
+  // Test hook (a real wait only): skip the polling, take the timeout path.
+  const bool hook = kHook && c_expire_site == where;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = hook ? 64 : 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (ld_volatile_u32(c.cta_abort)) return false;
     if (*reinterpret_cast<volatile unsigned int*>(&c.st->abort)) {
       *reinterpret_cast<volatile uint32_t*>(c.cta_abort) = 1u;
       return false;
     }
-    if (global_timer_ns() - t0 > c.timeout_ns) {
+    if (hook || global_timer_ns() - t0 > c.timeout_ns) {
       raise_abort(c, where);
       return false;
     }
@@ -84,18 +84,19 @@ __device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
 // compiled at one register count small.  Kernels that change their register
 // count per warpgroup (setmaxnreg) cannot call functions and use the inline
 // form (kInline = true).
+template <bool kHook>
 static __device__ __noinline__ bool wait_bar_slow(uint64_t* bar,
                                                    uint32_t parity,
                                                    WaitCtl c, uint32_t where) {
-  return wait_bar_poll(bar, parity, c, where);
+  return wait_bar_poll<kHook>(bar, parity, c, where);
 }
 
-template <bool kInline = false>
+template <bool kInline = false, bool kHook = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
                                          const WaitCtl& c, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
-  if constexpr (kInline) return wait_bar_poll(bar, parity, c, where);
-  else return wait_bar_slow(bar, parity, c, where);
+  if constexpr (kInline) return wait_bar_poll<kHook>(bar, parity, c, where);
+  else return wait_bar_slow<kHook>(bar, parity, c, where);
 }
 
 // Drain wait used only while a block is stopping: waits for an in-flight copy

@@ -367,7 +367,7 @@ __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
 // fit in L2 together, in rounds of gridDim.x items dealt to the blocks
 // alternately forwards and backwards, so that with items sorted by
 // decreasing cost every block gets a similar total.  Otherwise dynamically
-// (a.dynamic): block b starts with item b and then claims the next
+// (the DYN instantiations): block b starts with item b and then claims the next
 // unclaimed one from a counter in device memory, so that the head groups
 // cost no balance.  The counter belongs to this call (a slot of a ring the
 // host hands out); the last block to finish sets it back to zero for the
@@ -380,12 +380,11 @@ __device__ __forceinline__ int fwd_round_item(int r) {
 }
 
 // Item t of this block: the alternating rounds, computed locally, or (with
-// a.dynamic) the one the producer published.
-template <int S>
+// DYN) the one the producer published.
+template <bool DYN, int S>
 __device__ __forceinline__ bool fwd_take(FwdBars<S>* bars, int t, bool warp_wide,
-                                         const FwdArgs& a, const WaitCtl& wc,
-                                         uint32_t where, int& w) {
-  if (!a.dynamic) {
+                                         const WaitCtl& wc, uint32_t where, int& w) {
+  if constexpr (!DYN) {
     w = fwd_round_item(t);
     return true;
   }
@@ -404,7 +403,8 @@ __device__ __forceinline__ bool fwd_take(FwdBars<S>* bars, int t, bool warp_wide
 // phases run on across items, so the producer fetches the next item's Q and
 // K/V while the current one finishes, and the next item's first Q K^T
 // overlaps the softmax warps' epilogue.
-template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN, bool DYN,
+          bool HOOK>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int ti = 0; ok; ++ti) {
         FwdItem itm;
         int w;
-        if (!a.dynamic) {
+        if constexpr (!DYN) {
           // Alternating rounds: every role computes the same sequence.
           w = fwd_round_item(ti);
           if (w >= n_items) break;
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!VARLEN || itm.hi0 >= 0) break;
             w = (int)gridDim.x + (int)atomicAdd(a.work_next, 1u);
           }
-          ok = wait_bar<kInl>(&bars->sched_empty[ti & 1],
+          ok = wait_bar<kInl, HOOK>(&bars->sched_empty[ti & 1],
                               ((uint32_t)(ti >> 1) & 1u) ^ 1u, wc, kWFwdProdSched);
           if (!ok) break;
           *reinterpret_cast<volatile int*>(&bars->sched_item[ti & 1]) = w;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok || (t == 1 && itm.hi1 < 0)) break;
           uint32_t& q_cnt = t ? q_cnt1 : q_cnt0;
           // Q_t must no longer be read by the previous item's Q K^T.
-          ok = wait_bar<kInl>(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
+          ok = wait_bar<kInl, HOOK>(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars->q_full[t], kQKBytes);
 #pragma unroll
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int j = itm.jb; j <= itm.je && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv) {  // 0: K_j, 1: V_j
-            ok = wait_bar<kInl>(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
+            ok = wait_bar<kInl, HOOK>(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
             if (!ok) break;
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             const int boxes = kv ? L::kSub : kQKBoxes;
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       auto next_kv = [&](int& st) -> bool {
         st = stage;
-        const bool rr = wait_bar<kInl>(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
+        const bool rr = wait_bar<kInl, HOOK>(&bars->kv_full[stage], phase, wc, kWFwdMmaKV);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -594,16 +594,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       for (int ti = 0; ok; ++ti) {
         int w;
-        ok = fwd_take(bars, ti, false, a, wc, kWFwdMmaSched, w);
+        ok = fwd_take<DYN>(bars, ti, false, wc, kWFwdMmaSched, w);
         if (!ok || w >= n_items) break;
         const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
         if (VARLEN && itm.hi0 < 0) continue;  // empty item (alternating rounds)
         auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
         auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
-        ok = wait_bar<kInl>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
+        ok = wait_bar<kInl, HOOK>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
         ++q_cnt0;
         if (ok && itm.hi1 >= 0) {
-          ok = wait_bar<kInl>(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
+          ok = wait_bar<kInl, HOOK>(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
           ++q_cnt1;
         }
         int k_stage = 0;
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           int kn_stage = -1;
           // Tile 0: P V for key tile j, then Q K^T for key tile j+1.
           if (act0(j)) {
-            ok = wait_bar<kInl>(&bars->p_full[0], p_cnt0 & 1u, wc, kWFwdMmaP);
+            ok = wait_bar<kInl, HOOK>(&bars->p_full[0], p_cnt0 & 1u, wc, kWFwdMmaP);
             ++p_cnt0;
             if (!ok) break;
             tc_fence_after();
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mma_commit(&bars->o_done[0]);
           // Tile 1: the same; V_j is released after both tiles used it.
           if (act1(j)) {
-            ok = wait_bar<kInl>(&bars->p_full[1], p_cnt1 & 1u, wc, kWFwdMmaP);
+            ok = wait_bar<kInl, HOOK>(&bars->p_full[1], p_cnt1 & 1u, wc, kWFwdMmaP);
             ++p_cnt1;
             if (!ok) break;
             tc_fence_after();
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = run;
     for (int ti = 0; ok; ++ti) {
       int w;
-      ok = fwd_take(bars, ti, true, a, wc, kWFwdSmSched, w);
+      ok = fwd_take<DYN>(bars, ti, true, wc, kWFwdSmSched, w);
       if (!ok || w >= n_items) break;
       const FwdItem itm = fwd_item<CAUSAL, VARLEN>(w, n_tiles, n_pairs, a, tab);
       const int lo_t = t ? itm.lo1 : itm.lo0;
@@ -868,7 +868,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tmem_dealloc(tmem, 512);
   }
   // Every block has stopped claiming; the last one out resets the counter.
-  if (a.dynamic && threadIdx.x == 0) {
+  if (DYN && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.work_done, 1u) == gridDim.x - 1) {
       atomicExch(a.work_next, 0u);
@@ -877,13 +877,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN = false>
+template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN = false,
+          bool DYN = false, bool HOOK = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
   using L = FwdLayout<D>;
   static_assert(!VARLEN || (WINDOW && !FP8), "lengths run windowed, bf16");
-  auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8, VARLEN>;
+  static_assert(!DYN || !WINDOW, "banded calls use the alternating rounds");
+  // The failure-path test hook has its own instantiation, for d = 128 bf16
+  // without a window, lengths or the dynamic schedule only.
+  if constexpr (D == 128 && !WINDOW && !FP8 && !VARLEN && !DYN && !HOOK) {
+    if (a.hook)
+      return launch_fwd_t<D, CAUSAL, WINDOW, FP8, VARLEN, false, true>(
+          tq, tk, tv, a, BH, grid_blocks, stream);
+  }
+  // The dynamic schedule exists only without a window: the host asks for it
+  // (a.dynamic) only there.
+  if constexpr (!WINDOW && !DYN && !HOOK) {
+    if (a.dynamic)
+      return launch_fwd_t<D, CAUSAL, WINDOW, FP8, VARLEN, true>(tq, tk, tv, a, BH,
+                                                              grid_blocks, stream);
+  }
+  auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8, VARLEN, DYN, HOOK>;
   cudaError_t e;
   if constexpr (kSplitRegs) {
     // The register split inside the kernel assumes exactly kLaunchRegs per

@@ -33,10 +33,12 @@ struct FwdArgs {
   int n_sblk;
   // 1: blocks claim items from this call's work counter (a slot of a
   // zero-initialised ring, with its count of finished blocks; the last
-  // block resets both); 0: items are dealt in alternating rounds.
+  // block resets both); 0: items are dealt in alternating rounds.  Calls
+  // with a window always use 0.
   int dynamic;
   unsigned int* work_next;
   unsigned int* work_done;
+  int hook;           // 1: run the failure-path test hook instantiation
   DevState* st;
   uint64_t timeout_ns;
 };
@@ -67,6 +69,7 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   unsigned int* work_next;    // main kernel's work counter (workspace)
+  int hook;                   // 1: run the failure-path test hook instantiation
   DevState* st;
   uint64_t timeout_ns;
 };
