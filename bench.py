@@ -424,65 +424,106 @@ def run_ours(args, w, rank, world, local):
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    # -------- timed region: whole steps.  Events on the launching stream
-    # also mark each backward call and its main kernel, so the three
-    # backward launches are timed one by one (pre: call start to main start;
-    # post: main end to call end).
+    # -------- timed region: K whole steps, each bracketed by its own pair of
+    # events on the launching stream, with two more marking the end of the
+    # forward call and the main backward kernel (the library records those
+    # two around its launch), so every launch of a step is timed on the
+    # device.  By default each step is one CUDA graph (captured once per
+    # step index, so every step records its own events): a replay submits
+    # the four kernels at once and no host time falls inside a step.  When
+    # the step's inputs (Q, K, V, dO) are smaller than twice L2, a buffer of
+    # twice L2 is written before every step, outside its events.
     K = args.steps
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    flush = (torch.empty(max(1, l2 // 2), dtype=torch.float32, device=dev)
+             if in_bytes < 2 * l2 else None)
+    use_graph = not args.no_graph
+    graph_note = None
 
-    def ev_pair():
-        return (torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True))
-    main_ev = [ev_pair() for _ in range(K)]
-    bwd_ev = [ev_pair() for _ in range(K)]
+    def new_event():
+        if use_graph:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        return torch.cuda.Event(enable_timing=True)
+    try:
+        step_ev = [(new_event(), new_event()) for _ in range(K)]
+    except TypeError:            # a torch without external events
+        use_graph, graph_note = False, "torch.cuda.Event has no 'external'"
+        step_ev = [(new_event(), new_event()) for _ in range(K)]
+    fwd_end = [new_event() for _ in range(K)]
+    main_ev = [(new_event(), new_event()) for _ in range(K)]
     # torch creates the CUDA event lazily and only times events it recorded
     # itself: record each once here; the library re-records them later.
     for a, b in main_ev:
         a.record(stream)
         b.record(stream)
-    t_start, t_end = ev_pair()
+    torch.cuda.synchronize(dev)
+
+    def one_step(i):
+        s_ = torch.cuda.current_stream(dev)
+        fa_bwd_set_phase_events(*main_ev[i])
+        step_ev[i][0].record(s_)
+        fwd()
+        fwd_end[i].record(s_)
+        bwd()
+        step_ev[i][1].record(s_)
+
+    graphs = None
+    if use_graph:
+        try:
+            graphs = []
+            for i in range(K):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                    one_step(i)
+                graphs.append(g)
+            for _ in range(args.warmup):
+                graphs[0].replay()
+            torch.cuda.synchronize(dev)
+        except RuntimeError as ex:
+            graphs, use_graph = None, False
+            graph_note = "capture failed: %s" % str(ex).splitlines()[0]
+        finally:
+            fa_bwd_set_phase_events(None, None)
+    if fa_check_device_status(dev) != 0:
+        raise RuntimeError("device status error in the graph warm-up")
+
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
     barrier(world)
     torch.cuda.synchronize(dev)
-    t_start.record(stream)
     for i in range(K):
-        fa_bwd_set_phase_events(*main_ev[i])
-        fwd()
-        bwd_ev[i][0].record(stream)
-        bwd()
-        bwd_ev[i][1].record(stream)
-    t_end.record(stream)
+        if flush is not None:
+            flush.fill_(float(i))
+        if graphs is not None:
+            graphs[i].replay()
+        else:
+            one_step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     fa_bwd_set_phase_events(None, None)
     clocks = sampler.stop() if sampler else None
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error in the timed region")
-    step_ms_local = t_start.elapsed_time(t_end) / K
+
+    def mean_ms(pairs):
+        return sum(a.elapsed_time(b) for a, b in pairs) / K
+    step_ms_local = mean_ms(step_ev)
+    fwd_ms_local = mean_ms([(step_ev[i][0], fwd_end[i]) for i in range(K)])
     if idle:
         main_ms = pre_ms = post_ms = 0.0
     else:
-        main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / K
-        pre_ms = sum(bwd_ev[i][0].elapsed_time(main_ev[i][0])
-                     for i in range(K)) / K
-        post_ms = sum(main_ev[i][1].elapsed_time(bwd_ev[i][1])
-                      for i in range(K)) / K
+        main_ms = mean_ms(main_ev)
+        pre_ms = mean_ms([(fwd_end[i], main_ev[i][0]) for i in range(K)])
+        post_ms = mean_ms([(main_ev[i][1], step_ev[i][1]) for i in range(K)])
     step_ms = max_over_ranks(step_ms_local, world, dev)
-
-    # -------- forward alone (same inputs), for the forward-only figure
-    fw_s, fw_e = ev_pair()
-    for _ in range(max(1, args.warmup)):
-        fwd()
-    torch.cuda.synchronize(dev)
-    fw_s.record(stream)
-    for _ in range(K):
-        fwd()
-    fw_e.record(stream)
-    torch.cuda.synchronize(dev)
-    fwd_ms_local = fw_s.elapsed_time(fw_e) / K
     fwd_ms = max_over_ranks(fwd_ms_local, world, dev)
+    del graphs
+
+    def ev_pair():
+        return (torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True))
 
     # -------- FP8 forward (optional): Q, K quantised to E4M3 inside the call
     fp8 = None
@@ -627,6 +668,16 @@ def run_ours(args, w, rank, world, local):
                    if not args.varlen else
                    "contiguous batch entries of the one workload per rank")
         scaling = "strong"
+    l2_note = ("L2 flushed before every step (a %d MB write; the step's "
+               "Q, K, V, dO total %d MB, L2 %d MB)"
+               % (2 * l2 // 2**20, in_bytes // 2**20, l2 // 2**20)
+               if flush is not None else
+               "inputs larger than L2 (Q, K, V, dO total %d MB, L2 %d MB)"
+               % (in_bytes // 2**20, l2 // 2**20))
+    timing_note = ("one CUDA graph per step (fwd + bwd calls captured), "
+                   "events inside the graph" if use_graph else
+                   "eager calls, events on the stream"
+                   + ("" if graph_note is None else " (%s)" % graph_note))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -636,8 +687,8 @@ def run_ours(args, w, rank, world, local):
                         "d": w.d, "causal": w.causal, "scale": w.scale,
                         "qk_mult": w.qk_mult,
                         "per_gpu": per_gpu,
-                        "l2": "inputs larger than L2 (%d MB per Q tensor)" % (
-                            w.B * w.H * w.N * w.d * 2 // 2**20)},
+                        "l2": l2_note,
+                        "timing": timing_note},
                        **variant_config(w, args)),
         "fwd": {"value": fwd_tflops, "unit": "TFLOP/s", "ms": fwd_ms,
                 "frac_of_peak": fwd_tflops / world / peak_burst},
@@ -680,6 +731,8 @@ def main():
                     help="with several GPUs, run the whole workload on every "
                          "rank instead of splitting its heads")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls instead of one CUDA graph per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -318,7 +318,10 @@ fa_status fa_debug_expire_wait(void* stream);
  * records the caller-owned CUDA events `before_main` and `after_main`
  * (cudaEvent_t passed as void*) on its stream immediately before and after
  * the launch of its main kernel (the one running the tensor-core work), so
- * the caller can time that kernel alone.  NULL, NULL turns it off.
+ * the caller can time that kernel alone.  While the stream is being
+ * captured into a CUDA graph they are recorded as external events
+ * (cudaEventRecordExternal), so the graph records them each time it runs.
+ * NULL, NULL turns it off.
  */
 void fa_bwd_set_phase_events(void* before_main, void* after_main);
 

@@ -400,6 +400,18 @@ size_t fa_bwd_ext_workspace_size(int B, int H, int Hkv, int N, int d) {
 
 namespace {
 
+// Records a measurement event on `st`: as an external event node while the
+// stream is being captured into a CUDA graph (so that every run of the graph
+// records it), as a plain record otherwise.
+cudaError_t record_phase_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+             : cudaEventRecord(ev, st);
+}
+
 fa_status bwd_impl(const void* q, const void* k, const void* v,
                    const void* o, const float* lse, const void* dout,
                    void* dq, void* dk, void* dv, const int* seq_lens,
@@ -466,12 +478,12 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   const int elem_blocks = ctx->sm_count * 8;
   cudaError_t e = fa::launch_bwd_pre(a, d, elem_blocks, st);
   if (e == cudaSuccess && g_ev_before_main)
-    e = cudaEventRecord(g_ev_before_main, st);
+    e = record_phase_event(g_ev_before_main, st);
   if (e == cudaSuccess)
     e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, a, d, causal != 0,
                             ctx->sm_count, st);
   if (e == cudaSuccess && g_ev_after_main)
-    e = cudaEventRecord(g_ev_after_main, st);
+    e = record_phase_event(g_ev_after_main, st);
   if (e == cudaSuccess) e = fa::launch_bwd_post(a, d, elem_blocks, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
