@@ -424,14 +424,17 @@ def run_ours(args, w, rank, world, local):
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    # -------- timed region: K whole steps, each bracketed by its own pair of
-    # events on the launching stream, with two more marking the end of the
-    # forward call and the main backward kernel (the library records those
-    # two around its launch), so every launch of a step is timed on the
-    # device.  By default each step is one CUDA graph (captured once per
-    # step index, so every step records its own events): a replay submits
-    # the four kernels at once and no host time falls inside a step.  When
-    # the step's inputs (Q, K, V, dO) are smaller than twice L2, a buffer of
+    # -------- timed region.  Two sets of K steps, each step bracketed by
+    # its own pair of events on the launching stream.  The first set has
+    # nothing else between the four launches and gives the step time; the
+    # second also records an event after the forward call and two around
+    # the main backward kernel (the library records those two), which time
+    # every launch on its own but sit between the kernels (so they add
+    # their own cost and keep a kernel from being scheduled behind the one
+    # before it).  By default each step is one CUDA graph, captured once per
+    # step and set (so every step records its own events): a replay submits
+    # the launches at once and no host time falls inside a step.  When the
+    # step's inputs (Q, K, V, dO) are smaller than twice L2, a buffer of
     # twice L2 is written before every step, outside its events.
     K = args.steps
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -450,6 +453,7 @@ def run_ours(args, w, rank, world, local):
     except TypeError:            # a torch without external events
         use_graph, graph_note = False, "torch.cuda.Event has no 'external'"
         step_ev = [(new_event(), new_event()) for _ in range(K)]
+    ph_ev = [(new_event(), new_event()) for _ in range(K)]
     fwd_end = [new_event() for _ in range(K)]
     main_ev = [(new_event(), new_event()) for _ in range(K)]
     # torch creates the CUDA event lazily and only times events it recorded
@@ -459,32 +463,44 @@ def run_ours(args, w, rank, world, local):
         b.record(stream)
     torch.cuda.synchronize(dev)
 
-    def one_step(i):
+    def plain_step(i):
         s_ = torch.cuda.current_stream(dev)
-        fa_bwd_set_phase_events(*main_ev[i])
         step_ev[i][0].record(s_)
         fwd()
-        fwd_end[i].record(s_)
         bwd()
         step_ev[i][1].record(s_)
 
-    graphs = None
-    if use_graph:
+    def phase_step(i):
+        s_ = torch.cuda.current_stream(dev)
+        fa_bwd_set_phase_events(*main_ev[i])
         try:
-            graphs = []
-            for i in range(K):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, capture_error_mode="thread_local"):
-                    one_step(i)
-                graphs.append(g)
-            for _ in range(args.warmup):
-                graphs[0].replay()
-            torch.cuda.synchronize(dev)
-        except RuntimeError as ex:
-            graphs, use_graph = None, False
-            graph_note = "capture failed: %s" % str(ex).splitlines()[0]
+            ph_ev[i][0].record(s_)
+            fwd()
+            fwd_end[i].record(s_)
+            bwd()
+            ph_ev[i][1].record(s_)
         finally:
             fa_bwd_set_phase_events(None, None)
+
+    runs = {"plain": plain_step, "phase": phase_step}
+    if use_graph:
+        try:
+            graphs = {}
+            for name, fn in runs.items():
+                graphs[name] = []
+                for i in range(K):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                        fn(i)
+                    graphs[name].append(g)
+            for _ in range(args.warmup):
+                graphs["plain"][0].replay()
+            torch.cuda.synchronize(dev)
+            runs = {name: (lambda i, gs=gs: gs[i].replay())
+                    for name, gs in graphs.items()}
+        except RuntimeError as ex:
+            use_graph = False
+            graph_note = "capture failed: %s" % str(ex).splitlines()[0]
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error in the graph warm-up")
 
@@ -493,16 +509,13 @@ def run_ours(args, w, rank, world, local):
         sampler.start()
     barrier(world)
     torch.cuda.synchronize(dev)
-    for i in range(K):
-        if flush is not None:
-            flush.fill_(float(i))
-        if graphs is not None:
-            graphs[i].replay()
-        else:
-            one_step(i)
+    for name in ("plain", "phase"):
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(float(i))
+            runs[name](i)
     torch.cuda.synchronize(dev)
     barrier(world)
-    fa_bwd_set_phase_events(None, None)
     clocks = sampler.stop() if sampler else None
     if fa_check_device_status(dev) != 0:
         raise RuntimeError("device status error in the timed region")
@@ -510,16 +523,17 @@ def run_ours(args, w, rank, world, local):
     def mean_ms(pairs):
         return sum(a.elapsed_time(b) for a, b in pairs) / K
     step_ms_local = mean_ms(step_ev)
-    fwd_ms_local = mean_ms([(step_ev[i][0], fwd_end[i]) for i in range(K)])
+    phase_step_ms = mean_ms(ph_ev)
+    fwd_ms_local = mean_ms([(ph_ev[i][0], fwd_end[i]) for i in range(K)])
     if idle:
         main_ms = pre_ms = post_ms = 0.0
     else:
         main_ms = mean_ms(main_ev)
         pre_ms = mean_ms([(fwd_end[i], main_ev[i][0]) for i in range(K)])
-        post_ms = mean_ms([(main_ev[i][1], step_ev[i][1]) for i in range(K)])
+        post_ms = mean_ms([(main_ev[i][1], ph_ev[i][1]) for i in range(K)])
     step_ms = max_over_ranks(step_ms_local, world, dev)
     fwd_ms = max_over_ranks(fwd_ms_local, world, dev)
-    del graphs
+    del runs
 
     def ev_pair():
         return (torch.cuda.Event(enable_timing=True),
@@ -674,10 +688,13 @@ def run_ours(args, w, rank, world, local):
                if flush is not None else
                "inputs larger than L2 (Q, K, V, dO total %d MB, L2 %d MB)"
                % (in_bytes // 2**20, l2 // 2**20))
-    timing_note = ("one CUDA graph per step (fwd + bwd calls captured), "
-                   "events inside the graph" if use_graph else
-                   "eager calls, events on the stream"
-                   + ("" if graph_note is None else " (%s)" % graph_note))
+    timing_note = (("one CUDA graph per step (fwd + bwd calls captured), "
+                    "events inside the graph" if use_graph else
+                    "eager calls, events on the stream"
+                    + ("" if graph_note is None else " (%s)" % graph_note))
+                   + "; ms_per_step from steps with events only at their "
+                   "ends, the per-kernel times (bwd_ms, rooflines) from a "
+                   "second set of K steps with events between the kernels")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -698,12 +715,13 @@ def run_ours(args, w, rank, world, local):
         "roofline": roofline,
         "rooflines": rooflines,
         "bwd_ms": {"pre": pre_ms, "main": main_ms, "post": post_ms},
+        "ms_per_step_with_kernel_events": phase_step_ms,
         "cpu_baseline": cpu,
         "cpu_baseline_configs": cpu_configs,
         "cpu_baseline_1core": cpu_one,
         "e2e": e2e,
         "fwd_fp8": fp8,
-        "gpu_launches": 4 * K,
+        "gpu_launches": 8 * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
