@@ -436,11 +436,15 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   if ((s = device_ctx(&ctx)) != FA_OK) return s;
   const int BH = B * H, BHkv = B * Hkv;
   char* ws = static_cast<char*>(workspace);
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tk, k, BHkv, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tv, v, BHkv, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tdo, dout, BH, N, d)) != FA_OK) return s;
+  // dK, dV leave the main kernel in [32 rows x 64 columns] boxes, one per
+  // warp and 64-column half.
+  if ((s = make_tile_map(&tdk, dk, BHkv, N, d, 32)) != FA_OK) return s;
+  if ((s = make_tile_map(&tdv, dv, BHkv, N, d, 32)) != FA_OK) return s;
   if ((s = make_acc_map(&tdq, ws + w.dq_acc_off, BH, N, d)) != FA_OK) return s;
   fa::BwdArgs a{};
   a.o = static_cast<const __nv_bfloat16*>(o);
@@ -480,7 +484,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v,
   if (e == cudaSuccess && g_ev_before_main)
     e = record_phase_event(g_ev_before_main, st);
   if (e == cudaSuccess)
-    e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, a, d, causal != 0,
+    e = fa::launch_bwd_main(tq, tk, tv, tdo, tdq, tdk, tdv, a, d, causal != 0,
                             ctx->sm_count, st);
   if (e == cudaSuccess && g_ev_after_main)
     e = record_phase_event(g_ev_after_main, st);

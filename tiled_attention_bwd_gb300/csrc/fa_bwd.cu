@@ -124,15 +124,47 @@ enum : uint32_t {
   kWBwdMisaligned = 0x5A1,
 };
 
-// Row `krow` of dK or dV (key/value head bkv) from the TMEM accumulator at
-// column `tcol` (this thread's lane), times `mul`: rounded to bf16 into `out`,
-// or, when the group's query heads are split over several blocks, added in
-// fp32 into `acc` (vector atomics; rounded later by the post kernel).
-// Rows at or past `len` (the sequence's length) are not written.
+// The usual dK / dV epilogue: this thread's row of the TMEM accumulator at
+// column `tcol`, times `mul`, rounded to bf16 into a staging tile in shared
+// memory laid out as the TMA writes it (64-column sub-tiles `sub_stride`
+// bytes apart, 128-byte rows in the 128-byte swizzle, row `srow` of the
+// tile; a warp's 32 rows form one [32 x 64] box per sub-tile), from where
+// the warp's TMA stores send whole lines to global memory.  Per-thread
+// 16-byte stores of rows 2d bytes apart (the earlier form) kept the
+// load/store pipe busy for thousands of cycles per item and delayed the next
+// item's first P^T behind them.
 template <int D>
-__device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
-                                            float* acc, int bkv, int krow,
-                                            int N, int len, float mul) {
+__device__ __forceinline__ void kv_epilogue_stage(uint32_t tcol, uint8_t* tile,
+                                                  uint32_t sub_stride,
+                                                  uint32_t srow, float mul) {
+#pragma unroll 1
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(tcol + ch * 32, v);
+    tmem_wait_ld();
+    reg_fence32(v);
+    uint8_t* sub = tile + (ch >> 1) * sub_stride;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t col = (uint32_t)((ch & 1) * 32 + k * 8);
+      *reinterpret_cast<uint4*>(sub + sw128_offset(srow, col)) = make_uint4(
+          pack_bf16(__uint_as_float(v[8 * k + 0]) * mul, __uint_as_float(v[8 * k + 1]) * mul),
+          pack_bf16(__uint_as_float(v[8 * k + 2]) * mul, __uint_as_float(v[8 * k + 3]) * mul),
+          pack_bf16(__uint_as_float(v[8 * k + 4]) * mul, __uint_as_float(v[8 * k + 5]) * mul),
+          pack_bf16(__uint_as_float(v[8 * k + 6]) * mul, __uint_as_float(v[8 * k + 7]) * mul));
+    }
+  }
+}
+
+// Row `krow` of dK or dV (key/value head bkv) from the TMEM accumulator at
+// column `tcol` (this thread's lane), times `mul`, added in fp32 into `acc`
+// (vector atomics; rounded later by the post kernel): the epilogue when the
+// group's query heads are split over several blocks.  Rows at or past `len`
+// (the sequence's length) are not written.
+template <int D>
+__device__ __forceinline__ void kv_epilogue_atomic(uint32_t tcol, float* acc,
+                                                   int bkv, int krow, int N,
+                                                   int len, float mul) {
   const bool valid = krow < len;
   const size_t row = (size_t)bkv * N + (valid ? krow : 0);
 #pragma unroll 1
@@ -142,26 +174,13 @@ __device__ __forceinline__ void kv_epilogue(uint32_t tcol, __nv_bfloat16* out,
     tmem_wait_ld();
     reg_fence32(v);
     if (!valid) continue;
-    if (acc != nullptr) {
-      float4* dst = reinterpret_cast<float4*>(acc + row * D + ch * 32);
+    float4* dst = reinterpret_cast<float4*>(acc + row * D + ch * 32);
 #pragma unroll
-      for (int v4 = 0; v4 < 8; ++v4)
-        atomicAdd(dst + v4, make_float4(__uint_as_float(v[4 * v4]) * mul,
-                                        __uint_as_float(v[4 * v4 + 1]) * mul,
-                                        __uint_as_float(v[4 * v4 + 2]) * mul,
-                                        __uint_as_float(v[4 * v4 + 3]) * mul));
-    } else {
-      uint32_t pkv[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pkv[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul,
-                           __uint_as_float(v[2 * e + 1]) * mul);
-      uint4* dst = reinterpret_cast<uint4*>(out + row * D + ch * 32);
-#pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4)
-        dst[v4] = make_uint4(pkv[4 * v4], pkv[4 * v4 + 1], pkv[4 * v4 + 2],
-                             pkv[4 * v4 + 3]);
-    }
+    for (int v4 = 0; v4 < 8; ++v4)
+      atomicAdd(dst + v4, make_float4(__uint_as_float(v[4 * v4]) * mul,
+                                      __uint_as_float(v[4 * v4 + 1]) * mul,
+                                      __uint_as_float(v[4 * v4 + 2]) * mul,
+                                      __uint_as_float(v[4 * v4 + 3]) * mul));
   }
 }
 
@@ -262,6 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv,
                     const BwdArgs a) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -330,6 +351,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
       prefetch_tmap(&tm_dq);
+      prefetch_tmap(&tm_dk);
+      prefetch_tmap(&tm_dv);
       // Parity of the last load issued into each buffer (-1: none), so that
       // a stopping block can wait for its copies in flight.
       int k_par = -1, v_par = -1, q_par[2] = {-1, -1}, do_par = -1;
@@ -548,6 +571,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c = a.scale_log2;
     const uint64_t c2 = bcast2(c);
     bool ok = run;
+    bool stg_pending = false;  // this warp's dK rows are being stored from dS
     uint32_t g = 0;
     for (int t = 0; ok; ++t) {
       int w;
@@ -641,6 +665,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = wait_bar_warp(&bars->dp_full, par, wc, kWBwdCmpDp);
         if (ok && gi > 0) ok = wait_bar_warp(&bars->ds_free, par ^ 1u, wc, kWBwdCmpDsFree);
         if (!ok) break;
+        if (stg_pending) {  // the TMA has read this warp's dK rows from dS
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          stg_pending = false;
+        }
         tc_fence_after();
         // dS^T goes to smem (read MN-major as dS by the dQ MMA) and, packed to
         // bf16 pairs, into TMEM columns [128, 192) over dP^T values already
@@ -688,12 +717,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait_bar_warp(&bars->acc_done, (uint32_t)t & 1u, wc, kWBwdCmpAcc);
       if (!ok) break;
       tc_fence_after();
-      kv_epilogue<D>(tl + 256, a.dk, a.nsplit > 1 ? a.dk_acc : nullptr, itm.bkv,
-                     j * kTile + r, a.N, itm.len, a.scale);
-      tc_fence_before();
-      warp_arrive(&bars->acc_free);
+      if (a.nsplit > 1) {
+        kv_epilogue_atomic<D>(tl + 256, a.dk_acc, itm.bkv, j * kTile + r, a.N,
+                              itm.len, a.scale);
+        tc_fence_before();
+        warp_arrive(&bars->acc_free);
+      } else {
+        // Staged in the dS tile: its last reader, the item's last dQ MMA, is
+        // complete (acc_done follows it), and each warp owns its 32 rows
+        // there.  The stores clip rows past N; rows past a sequence's end
+        // hold zeros (no visible query) and are cleared again by the post
+        // kernel.
+        kv_epilogue_stage<D>(tl + 256, ds_s, kSubTileBytes, (uint32_t)r, a.scale);
+        tc_fence_before();
+        warp_arrive(&bars->acc_free);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int sb = 0; sb < L::kSub; ++sb)
+            tma_store_3d(&tm_dk, ds_s + sb * kSubTileBytes + quarter * 32 * 128,
+                         sb * 64, j * kTile + quarter * 32, itm.bkv);
+          bulk_commit_group();
+        }
+        stg_pending = true;
+      }
       g += (uint32_t)itm.nq;
     }
+    if (lane == 0) bulk_wait_all();  // dK stores complete before exit
   } else if (warp < 8) {
     // ------------------------------------- dQ drain (thread = query row)
     // dQ_i leaves TMEM into registers (then the columns are released) and is
@@ -709,6 +760,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* const stg_w = stg_s + quarter * 2 * L::kStgBoxBytes;
     constexpr int kBoxes = D / 32;
     int gb = 0;                                      // boxes staged so far
+    bool stg_busy = false;  // both boxes hold dV rows being stored
     bool ok = run;
     uint32_t g = 0;
     for (int t = 0; ok; ++t) {
@@ -734,7 +786,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int b = 0; b < kBoxes; ++b, ++gb) {
           uint8_t* const buf = stg_w + (gb & 1) * L::kStgBoxBytes;
-          if (gb >= 2) {
+          if (stg_busy) {  // the dV stores have read both boxes
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            stg_busy = false;
+          } else if (gb >= 2) {
             if (lane == 0) bulk_wait_read_allbut1();  // box gb-2 has been read
             __syncwarp();
           }
@@ -757,13 +813,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait_bar_warp(&bars->acc_done, (uint32_t)t & 1u, wc, kWBwdDqAcc);
       if (!ok) break;
       tc_fence_after();
-      kv_epilogue<D>(tl + 256 + D, a.dv, a.nsplit > 1 ? a.dv_acc : nullptr,
-                     itm.bkv, itm.j * kTile + r, a.N, itm.len, 1.0f);
-      tc_fence_before();
-      warp_arrive(&bars->acc_free);
+      if (a.nsplit > 1) {
+        kv_epilogue_atomic<D>(tl + 256 + D, a.dv_acc, itm.bkv, itm.j * kTile + r,
+                              a.N, itm.len, 1.0f);
+        tc_fence_before();
+        warp_arrive(&bars->acc_free);
+      } else {
+        // Staged in this warp's two boxes once its dQ adds have read them.
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        kv_epilogue_stage<D>(tl + 256 + D, stg_w, L::kStgBoxBytes, (uint32_t)lane,
+                             1.0f);
+        tc_fence_before();
+        warp_arrive(&bars->acc_free);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int sb = 0; sb < L::kSub; ++sb)
+            tma_store_3d(&tm_dv, stg_w + sb * L::kStgBoxBytes, sb * 64,
+                         itm.j * kTile + quarter * 32, itm.bkv);
+          bulk_commit_group();
+        }
+        stg_busy = true;
+      }
       g += (uint32_t)itm.nq;
     }
-    if (lane == 0) bulk_wait_all();  // accumulator adds complete before exit
+    if (lane == 0) bulk_wait_all();  // dQ adds and dV stores complete before exit
   }
 
   tc_fence_before();
@@ -966,15 +1042,16 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a, int d) {
 template <int D, bool CAUSAL, bool VARLEN, bool HOOK = false>
 cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
-                          const CUtensorMap& tdq, const BwdArgs& a,
+                          const CUtensorMap& tdq, const CUtensorMap& tdk,
+                          const CUtensorMap& tdv, const BwdArgs& a,
                           int grid_blocks, cudaStream_t stream) {
   using L = BwdLayout<D>;
   // The failure-path test hook has its own instantiation, for d = 128
   // without per-sequence lengths only.
   if constexpr (D == 128 && !VARLEN && !HOOK) {
     if (a.hook)
-      return launch_main_t<D, CAUSAL, VARLEN, true>(tq, tk, tv, tdo, tdq, a,
-                                                    grid_blocks, stream);
+      return launch_main_t<D, CAUSAL, VARLEN, true>(tq, tk, tv, tdo, tdq, tdk,
+                                                    tdv, a, grid_blocks, stream);
   }
   auto kern = bwd_main_kernel<D, CAUSAL, VARLEN, HOOK>;
   cudaError_t e = cudaFuncSetAttribute(
@@ -983,7 +1060,8 @@ cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk,
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const long long n_items = (long long)a.BHkv * a.nsplit * n_tiles;
   const int blocks = n_items < grid_blocks ? (int)n_items : grid_blocks;
-  kern<<<blocks, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  kern<<<blocks, kBwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq,
+                                                        tdk, tdv, a);
   return cudaGetLastError();
 }
 
@@ -1000,22 +1078,23 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
 
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdq, const BwdArgs& a, int d,
+                            const CUtensorMap& tdq, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, const BwdArgs& a, int d,
                             bool causal, int grid_blocks, cudaStream_t stream) {
   const bool vl = a.seq_lens != nullptr;
   const int gb = grid_blocks;
   if (d == 128) {
     if (causal)
-      return vl ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
-                : launch_main_t<128, true, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
-    return vl ? launch_main_t<128, false, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
-              : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
+      return vl ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream)
+                : launch_main_t<128, true, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream);
+    return vl ? launch_main_t<128, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream)
+              : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream);
   }
   if (causal)
-    return vl ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
-              : launch_main_t<64, true, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
-  return vl ? launch_main_t<64, false, true>(tq, tk, tv, tdo, tdq, a, gb, stream)
-            : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdq, a, gb, stream);
+    return vl ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream)
+              : launch_main_t<64, true, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream);
+  return vl ? launch_main_t<64, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream)
+            : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, gb, stream);
 }
 
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,

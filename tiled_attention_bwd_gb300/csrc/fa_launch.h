@@ -93,7 +93,8 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
 // Persistent: min(work items, grid_blocks) blocks, one per SM.
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdq, const BwdArgs& a, int d,
+                            const CUtensorMap& tdq, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, const BwdArgs& a, int d,
                             bool causal, int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, int d, int grid_blocks,
                             cudaStream_t stream);

@@ -92,6 +92,18 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map,
       "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 3-D tiled store of one shared-memory box into global memory (rows past
+// the tensor's extent are not written).  Tracked by the bulk async-group of
+// this thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map,
+                                             const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group "
+      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
