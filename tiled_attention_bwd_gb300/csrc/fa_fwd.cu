@@ -55,7 +55,8 @@ static_assert(!kSplitRegs || 2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <=
               "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 
-// Shared memory: two Q tiles and a ring of K/V tiles, all 128 rows.
+// Shared memory: three Q tile buffers (see q_buf) and a ring of K/V tiles,
+// all 128 rows.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_t (bf16 pairs) is written over the first 64 columns of S_t.
 //
@@ -72,7 +73,8 @@ struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 128) ? 4 : 6;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kQBufs = 3;
+  static constexpr int kKVOff = kQBufs * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
 };
@@ -82,8 +84,8 @@ constexpr int kFwdBarBytes = 256;
 
 template <int STAGES>
 struct FwdBars {
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
+  uint64_t q_full[3];    // per Q buffer
+  uint64_t q_empty[3];
   uint64_t kv_full[STAGES];
   uint64_t kv_empty[STAGES];
   uint64_t s_full[2];
@@ -110,6 +112,18 @@ enum : uint32_t {
   kWFwdSmS = 0x301,
   kWFwdSmO = 0x302,
 };
+
+// Q buffer of tile t (0, 1) of the n-th item (with work) a block runs.
+// Tile 0 takes the buffer the item before left spare, tile 1 that item's
+// tile-0 buffer, which is freed a key tile before its tile-1 buffer (causal
+// pairs end one key tile apart).  So both loads of the next item can be
+// issued while the current item's last key tiles run, instead of waiting
+// for its tile 1 to let go of its buffer: buffers (t0, t1, spare) run
+// (0, 1, 2), (2, 0, 1), (1, 2, 0), ...
+__device__ __forceinline__ int q_buf(uint32_t n, int t) {
+  const int r = (int)(n % 3u);
+  return (t == 0 ? 3 - r : 4 - r) % 3;
+}
 
 // S_t = Q_t K^T: M = N = 128, K = d; both operands K-major in smem.  The
 // descriptors are those of the tiles' first bytes; each 16-wide K step is
@@ -436,9 +450,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (threadIdx.x == 0) {
     bars->abort = *reinterpret_cast<volatile unsigned int*>(&a.st->abort);
+    for (int b = 0; b < L::kQBufs; ++b) {
+      mbar_init(&bars->q_full[b], 1);
+      mbar_init(&bars->q_empty[b], 1);
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->q_full[t], 1);
-      mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);   // one arrival per warp
       mbar_init(&bars->o_done[t], 1);
@@ -479,7 +495,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int s = 0; s < S; ++s) last_par[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t q_cnt0 = 0, q_cnt1 = 0;   // loads issued into each Q buffer
+      // Per Q buffer (bit b): parity of the loads issued into it, and
+      // whether it has had one.
+      uint32_t q_par = 0, q_used = 0;
+      uint32_t n_done = 0;   // items with work so far
       bool ok = true;
       for (int ti = 0; ok; ++ti) {
         FwdItem itm;
@@ -511,18 +530,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || (t == 1 && itm.hi1 < 0)) break;
-          uint32_t& q_cnt = t ? q_cnt1 : q_cnt0;
-          // Q_t must no longer be read by the previous item's Q K^T.
-          ok = wait_bar<kInl, HOOK>(&bars->q_empty[t], (q_cnt & 1u) ^ 1u, wc, kWFwdProdQ);
+          const int b = q_buf(n_done, t);
+          // The buffer must no longer be read by an earlier item's Q K^T.
+          ok = wait_bar<kInl, HOOK>(&bars->q_empty[b], ((q_par >> b) & 1u) ^ 1u, wc,
+                                    kWFwdProdQ);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->q_full[t], kQKBytes);
+          mbar_arrive_expect_tx(&bars->q_full[b], kQKBytes);
 #pragma unroll
           for (int sb = 0; sb < kQKBoxes; ++sb)
-            tma_load_3d(smem + L::kQOff + t * L::kTileBytes + sb * kSubTileBytes,
-                        &tm_q, &bars->q_full[t], sb * 64,
+            tma_load_3d(smem + L::kQOff + b * L::kTileBytes + sb * kSubTileBytes,
+                        &tm_q, &bars->q_full[b], sb * 64,
                         (t ? itm.qt1 : itm.qt0) * kTile, itm.bh);
-          ++q_cnt;
+          q_par ^= 1u << b;
+          q_used |= 1u << b;
         }
+        ++n_done;
         for (int j = itm.jb; j <= itm.je && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv) {  // 0: K_j, 1: V_j
             ok = wait_bar<kInl, HOOK>(&bars->kv_empty[stage], phase ^ 1u, wc, kWFwdProdEmpty);
@@ -545,8 +567,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) {
         // Stopping: let every copy this thread started land before exit.
-        if (q_cnt0 > 0) drain_bar<kInl>(&bars->q_full[0], (q_cnt0 - 1) & 1u, a.timeout_ns);
-        if (q_cnt1 > 0) drain_bar<kInl>(&bars->q_full[1], (q_cnt1 - 1) & 1u, a.timeout_ns);
+        for (int b = 0; b < L::kQBufs; ++b)
+          if ((q_used >> b) & 1u)
+            drain_bar<kInl>(&bars->q_full[b], ((q_par >> b) & 1u) ^ 1u, a.timeout_ns);
         for (int s = 0; s < S; ++s)
           if (last_par[s] >= 0)
             drain_bar<kInl>(&bars->kv_full[s], (uint32_t)last_par[s], a.timeout_ns);
@@ -564,14 +587,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint64_t q_desc0 = sdesc_sw128(q_base, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(kv_addr, 16, 1024);
       const uint64_t kv_desc_v = sdesc_sw128(kv_addr, kSubTileBytes, 1024);
-      auto q_desc = [&](int t) { return sdesc_adv(q_desc0, t * L::kTileBytes); };
+      auto q_desc = [&](int b) { return sdesc_adv(q_desc0, b * L::kTileBytes); };
       auto k_desc = [&](int st) { return sdesc_adv(kv_desc_k, st * L::kTileBytes); };
       auto v_desc = [&](int st) { return sdesc_adv(kv_desc_v, st * L::kTileBytes); };
       auto tS = [&](int t) { return tmem + (uint32_t)(t * 128); };
       auto tO = [&](int t) { return tmem + (uint32_t)(256 + t * D); };
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t q_cnt0 = 0, q_cnt1 = 0, p_cnt0 = 0, p_cnt1 = 0;
+      uint32_t q_par = 0;    // per Q buffer (bit b): parity of its next load
+      uint32_t n_done = 0;   // items with work so far
+      uint32_t p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
       auto next_kv = [&](int& st) -> bool {
         st = stage;
@@ -582,15 +607,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         return rr;
       };
-      // Q K^T for tile t and key tile x; after the tile's last one (hi_t),
-      // Q_t is released to the producer (in-order completion).
-      auto qk = [&](int t, int x, int hi_t, int k_st) {
+      // Q K^T for tile t (in Q buffer b) and key tile x; after the tile's
+      // last one (hi_t), the buffer is released to the producer (in-order
+      // completion).
+      auto qk = [&](int t, int b, int x, int hi_t, int k_st) {
         if constexpr (FP8)
-          issue_qk_fp8(tS(t), q_desc(t), k_desc(k_st));
+          issue_qk_fp8(tS(t), q_desc(b), k_desc(k_st));
         else
-          issue_qk<D>(tS(t), q_desc(t), k_desc(k_st));
+          issue_qk<D>(tS(t), q_desc(b), k_desc(k_st));
         mma_commit(&bars->s_full[t]);
-        if (x == hi_t) mma_commit(&bars->q_empty[t]);
+        if (x == hi_t) mma_commit(&bars->q_empty[b]);
       };
       for (int ti = 0; ok; ++ti) {
         int w;
@@ -600,18 +626,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (VARLEN && itm.hi0 < 0) continue;  // empty item (alternating rounds)
         auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
         auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
-        ok = wait_bar<kInl, HOOK>(&bars->q_full[0], q_cnt0 & 1u, wc, kWFwdMmaQ);
-        ++q_cnt0;
+        const int qb0 = q_buf(n_done, 0), qb1 = q_buf(n_done, 1);
+        ++n_done;
+        ok = wait_bar<kInl, HOOK>(&bars->q_full[qb0], (q_par >> qb0) & 1u, wc, kWFwdMmaQ);
+        q_par ^= 1u << qb0;
         if (ok && itm.hi1 >= 0) {
-          ok = wait_bar<kInl, HOOK>(&bars->q_full[1], q_cnt1 & 1u, wc, kWFwdMmaQ);
-          ++q_cnt1;
+          ok = wait_bar<kInl, HOOK>(&bars->q_full[qb1], (q_par >> qb1) & 1u, wc, kWFwdMmaQ);
+          q_par ^= 1u << qb1;
         }
         int k_stage = 0;
         if (ok) ok = next_kv(k_stage);
         if (!ok) break;
         tc_fence_after();
-        qk(0, itm.jb, itm.hi0, k_stage);
-        if (act1(itm.jb)) qk(1, itm.jb, itm.hi1, k_stage);
+        qk(0, qb0, itm.jb, itm.hi0, k_stage);
+        if (act1(itm.jb)) qk(1, qb1, itm.jb, itm.hi1, k_stage);
         mma_commit(&bars->kv_empty[k_stage]);
         for (int j = itm.jb; j <= itm.je && ok; ++j) {
           int v_stage = 0;
@@ -634,7 +662,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tc_fence_after();
           }
           if (act0(j + 1))
-            qk(0, j + 1, itm.hi0, kn_stage);
+            qk(0, qb0, j + 1, itm.hi0, kn_stage);
           else if (j == itm.hi0)
             mma_commit(&bars->o_done[0]);
           // Tile 1: the same; V_j is released after both tiles used it.
@@ -647,7 +675,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           mma_commit(&bars->kv_empty[v_stage]);
           if (act1(j + 1))
-            qk(1, j + 1, itm.hi1, kn_stage);
+            qk(1, qb1, j + 1, itm.hi1, kn_stage);
           else if (j == itm.hi1)
             mma_commit(&bars->o_done[1]);
           if (kn_stage >= 0) mma_commit(&bars->kv_empty[kn_stage]);
