@@ -119,7 +119,9 @@ enum : uint32_t {
 // pairs end one key tile apart).  So both loads of the next item can be
 // issued while the current item's last key tiles run, instead of waiting
 // for its tile 1 to let go of its buffer: buffers (t0, t1, spare) run
-// (0, 1, 2), (2, 0, 1), (1, 2, 0), ...
+// (0, 1, 2), (2, 0, 1), (1, 2, 0), ...  The banded (WINDOW) kernels keep
+// tile t in buffer t: the rotation's state in their 96-register control
+// warps cost them 3-4%.
 __device__ __forceinline__ int q_buf(uint32_t n, int t) {
   const int r = (int)(n % 3u);
   return (t == 0 ? 3 - r : 4 - r) % 3;
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || (t == 1 && itm.hi1 < 0)) break;
-          const int b = q_buf(n_done, t);
+          const int b = WINDOW ? t : q_buf(n_done, t);
           // The buffer must no longer be read by an earlier item's Q K^T.
           ok = wait_bar<kInl, HOOK>(&bars->q_empty[b], ((q_par >> b) & 1u) ^ 1u, wc,
                                     kWFwdProdQ);
@@ -626,7 +628,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (VARLEN && itm.hi0 < 0) continue;  // empty item (alternating rounds)
         auto act0 = [&](int x) { return x <= itm.hi0; };  // x >= lo0 = jb
         auto act1 = [&](int x) { return x >= itm.lo1 && x <= itm.hi1; };
-        const int qb0 = q_buf(n_done, 0), qb1 = q_buf(n_done, 1);
+        const int qb0 = WINDOW ? 0 : q_buf(n_done, 0);
+        const int qb1 = WINDOW ? 1 : q_buf(n_done, 1);
         ++n_done;
         ok = wait_bar<kInl, HOOK>(&bars->q_full[qb0], (q_par >> qb0) & 1u, wc, kWFwdMmaQ);
         q_par ^= 1u << qb0;
