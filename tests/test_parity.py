@@ -84,6 +84,10 @@ SMALL = [
     (2, 1, 100, 128, False), (1, 1, 200, 64, True),
     (1, 3, 333, 128, True), (2, 2, 333, 128, False),
     (1, 1, 1000, 64, True),
+    # With fewer pairs of Q tiles than SMs (every case above) the forward's
+    # work items are single Q tiles; these have more, so they run the pair
+    # items, with a ragged last tile.
+    (2, 80, 333, 128, True), (2, 80, 200, 64, False),
 ]
 
 

@@ -110,6 +110,16 @@ void fwd_schedule(int BH, int N, int d, fa::FwdArgs& a) {
   a.dynamic = 1;
 }
 
+// Forward work items of one Q tile instead of two when a problem has fewer
+// pairs of Q tiles than SMs (then most SMs would idle); the two tiles of a
+// pair share their K/V loads, so pairs stay the unit otherwise.  The
+// kernels with per-sequence lengths keep pairs (their balanced item table
+// counts pairs).
+int single_tile_items(int BH, int N, int sm_count, bool lengths) {
+  const long long pairs = (long long)BH * (((N + fa::kTile - 1) / fa::kTile + 1) / 2);
+  return (!lengths && pairs < sm_count) ? 1 : 0;
+}
+
 fa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   std::call_once(g_encode_once, [] {
     void* p = nullptr;
@@ -345,6 +355,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   a.window = (seq_lens && win < 0) ? N - 1 : win;
   a.seq_lens = seq_lens;
   fwd_schedule(BH, N, d, a);
+  a.single = single_tile_items(BH, N, ctx->sm_count, seq_lens != nullptr);
   a.scale_log2 = scale * fa::kLog2e;
   a.st = ctx->state;
   a.timeout_ns = kernel_timeout();
@@ -596,6 +607,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.Hkv = H;
   a.window = -1;
   fwd_schedule(BH, N, d, a);
+  a.single = single_tile_items(BH, N, ctx->sm_count, false);
   a.scale_log2 = scale * fa::kLog2e;
   a.q_scale = sq;
   a.k_scale = sk;

@@ -356,8 +356,9 @@ __device__ __forceinline__ FwdItem fwd_item(int w, int n_tiles, int n_pairs,
   }
   const int b = it.bh / a.H, h = it.bh - b * a.H;
   it.kvh = b * a.Hkv + h / (a.H / a.Hkv);
-  it.qt0 = 2 * pair;
-  it.qt1 = 2 * pair + 1;
+  // A single-tile item has no tile 1 (qt1 past the last tile).
+  it.qt0 = a.single ? pair : 2 * pair;
+  it.qt1 = a.single ? n_tiles : 2 * pair + 1;
   // With per-sequence lengths, tiles at or past the sequence's end are not
   // visited; an item with no tile left is empty (hi0 = -1) for every role.
   it.len = VARLEN ? seq_len_of(a.seq_lens, b, a.N) : a.N;
@@ -439,7 +440,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int n_pairs = (n_tiles + 1) / 2;
+  // Work items ("pairs" below) per head: pairs of Q tiles, or single tiles.
+  const int n_pairs = a.single ? n_tiles : (n_tiles + 1) / 2;
   int n_items = a.BH * n_pairs;
   const int* tab = nullptr;
   if constexpr (VARLEN) {
@@ -942,7 +944,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     if (fa_attr.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   }
   const int n_tiles = (a.N + kTile - 1) / kTile;
-  const int n_pairs = (n_tiles + 1) / 2;
+  const int n_pairs = a.single ? n_tiles : (n_tiles + 1) / 2;
   FwdArgs args = a;
   size_t smem_bytes = L::kSmemBytes;
   args.sched = 0;

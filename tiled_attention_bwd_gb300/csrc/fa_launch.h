@@ -36,6 +36,9 @@ struct FwdArgs {
   // block resets both); 0: items are dealt in alternating rounds.  Calls
   // with a window always use 0.
   int dynamic;
+  // 1: each work item is one Q tile instead of a pair (set when a problem
+  // has fewer pairs than SMs; never with per-sequence lengths).
+  int single;
   unsigned int* work_next;
   unsigned int* work_done;
   int hook;           // 1: run the failure-path test hook instantiation
