@@ -197,7 +197,9 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v,
  *   - Same arguments as fa_fwd plus a workspace of
  *     fa_fwd_fp8_workspace_size(B, H, N, d) bytes (E4M3 copies of Q and K
  *     and their scales), 256-byte aligned, owned by the caller.
- *   - d = 128 only (other d: FA_ERR_UNSUPPORTED).
+ *   - d = 64 or 128.  The E4M3 copies have rows of 128 bytes; at d = 64 the
+ *     upper 64 bytes of each row are zero, so Q K^T runs as the d = 128
+ *     product and P V as the d = 64 one.
  */
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d);
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,

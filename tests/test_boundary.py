@@ -252,7 +252,6 @@ def _fwd_fp8(lib, ptr=256, lse=16, ws=256, ws_bytes=1 << 40, B=1, H=1, N=128,
 
 
 def test_fp8_forward_argument_checks(lib):
-    assert _fwd_fp8(lib, d=64) == UNSUPPORTED
     assert _fwd_fp8(lib, d=96) == UNSUPPORTED
     assert _fwd_fp8(lib, scale=0.0) == INVALID
     assert _fwd_fp8(lib, ptr=0) == INVALID
@@ -269,12 +268,14 @@ def test_fp8_forward_argument_checks(lib):
 
 
 @pytest.mark.parametrize("B,H,N,d", [(4, 64, 4096, 128), (1, 3, 333, 128),
-                                     (2, 2, 1, 128)])
+                                     (2, 2, 1, 128), (2, 8, 512, 64),
+                                     (1, 3, 333, 64)])
 def test_fp8_workspace_size(lib, B, H, N, d):
     nsb = 8 * ((N + 127) // 128)
-    expect = 2 * _align(B * H * N * d) + 2 * _align(B * H * nsb * 4)
+    # E4M3 rows are 128 bytes at either d (zero-padded at d = 64)
+    expect = 2 * _align(B * H * N * 128) + 2 * _align(B * H * nsb * 4)
     assert lib.fa_fwd_fp8_workspace_size(B, H, N, d) == expect
-    assert lib.fa_fwd_fp8_workspace_size(B, H, N, 64) == 0
+    assert lib.fa_fwd_fp8_workspace_size(B, H, N, 96) == 0
 
 
 def _step_host(lib, ptr=256, scratch=256, scratch_bytes=1 << 40, B=2, H=8,

@@ -62,21 +62,24 @@ def check_forward(o, lse, o_ref, lse_ref, tag):
     assert le <= LSE_MAX_ABS, "%s LSE max-abs %.3g" % (tag, le)
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,H,N,causal,mult", [(1, 1, 128, False, 1.0),
                                                (1, 2, 256, True, 1.0),
                                                (2, 2, 384, True, 2.0),
                                                (1, 3, 333, False, 1.0),
                                                (1, 2, 1000, True, 1.0),
-                                               (1, 1, 17, True, 1.0)])
-def test_fp8_forward_every_element(B, H, N, causal, mult):
+                                               (1, 1, 17, True, 1.0),
+                                               (2, 8, 512, False, 1.0)])
+def test_fp8_forward_every_element(B, H, N, causal, mult, d):
     dev = torch.device("cuda:0")
-    inp = make_inputs(B, H, N, 128, seed=77 + N, qk_mult=mult)
-    scale = default_scale(128)
+    inp = make_inputs(B, H, N, d, seed=77 + N + d, qk_mult=mult)
+    scale = default_scale(d)
     o, lse = fa_fwd_fp8(*(inp[n].to(dev) for n in ("q", "k", "v")), causal,
                         scale)
     assert fa_check_device_status(dev) == 0
     o_ref, lse_ref = ofp8.fwd_fp8(inp["q"], inp["k"], inp["v"], causal, scale)
-    check_forward(o, lse, o_ref, lse_ref, "%dx%dx%d causal=%d" % (B, H, N, causal))
+    check_forward(o, lse, o_ref, lse_ref,
+                  "%dx%dx%dx%d causal=%d" % (B, H, N, d, causal))
 
 
 def test_fp8_forward_full_size_sampled_heads():

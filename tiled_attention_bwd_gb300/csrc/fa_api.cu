@@ -174,8 +174,8 @@ fa_status make_acc_map(CUtensorMap* m, const void* base, int BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D view [BH][N][d] of an E4M3 tensor (one byte per element); box = 128
-// rows x 128 bytes (d = 128), 128-byte swizzle.  Rows past N read as zeros.
+// 3-D view [BH][N][row_bytes] of an E4M3 tensor (one byte per element);
+// box = 128 rows x 128 bytes, 128-byte swizzle.  Rows past N read as zeros.
 fa_status make_fp8_map(CUtensorMap* m, const void* base, int BH, int N,
                        int d) {
   PFN_cuTensorMapEncodeTiled_v12000 fn;
@@ -280,14 +280,18 @@ struct Fp8Layout {
   size_t q8_off, k8_off, sq_off, sk_off, total;
 };
 
-// E4M3 Q | E4M3 K (B*H*N*d bytes each) | Q scales | K scales
+// E4M3 rows of the FP8 forward: 128 bytes whatever d (d = 64 rows carry 64
+// zero bytes, so that Q K^T is the d = 128 product).
+constexpr int kFp8RowBytes = 128;
+
+// E4M3 Q | E4M3 K (B*H*N rows of kFp8RowBytes each) | Q scales | K scales
 // ([B*H][scale_blocks(N)] float32), each 256-byte aligned.
-Fp8Layout fp8_layout(int B, int H, int N, int d) {
+Fp8Layout fp8_layout(int B, int H, int N, int /*d*/) {
   const size_t BH = (size_t)B * H;
   Fp8Layout w;
   w.q8_off = 0;
-  w.k8_off = align_up(BH * N * d, 256);
-  w.sq_off = w.k8_off + align_up(BH * N * d, 256);
+  w.k8_off = align_up(BH * N * kFp8RowBytes, 256);
+  w.sq_off = w.k8_off + align_up(BH * N * kFp8RowBytes, 256);
   w.sk_off = w.sq_off + align_up(BH * scale_blocks(N) * sizeof(float), 256);
   w.total = w.sk_off + align_up(BH * scale_blocks(N) * sizeof(float), 256);
   return w;
@@ -540,8 +544,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
 
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {
   bool empty = false;
-  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty || d != 128)
-    return 0;
+  if (check_shape(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
   return fp8_layout(B, H, N, d).total;
 }
 
@@ -557,7 +560,7 @@ fa_status fa_quantize_e4m3(const void* x, void* codes, float* scales, int BH,
   if ((s = device_ctx(&ctx)) != FA_OK) return s;
   cudaError_t e = fa::launch_quant_e4m3(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(codes),
-      scales, BH, N, d, scale_blocks(N), ctx->sm_count * 8,
+      scales, BH, N, d, scale_blocks(N), d, ctx->sm_count * 8,
       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -569,7 +572,6 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   bool empty = false;
   fa_status s = check_shape(B, H, N, d, causal, scale, &empty);
   if (s != FA_OK || empty) return s;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || !aligned(lse, 4))
@@ -586,17 +588,17 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   float* sq = reinterpret_cast<float*>(ws + w.sq_off);
   float* sk = reinterpret_cast<float*>(ws + w.sk_off);
   CUtensorMap tq, tk, tv;
-  if ((s = make_fp8_map(&tq, q8, BH, N, d)) != FA_OK) return s;
-  if ((s = make_fp8_map(&tk, k8, BH, N, d)) != FA_OK) return s;
+  if ((s = make_fp8_map(&tq, q8, BH, N, kFp8RowBytes)) != FA_OK) return s;
+  if ((s = make_fp8_map(&tk, k8, BH, N, kFp8RowBytes)) != FA_OK) return s;
   if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int nsb = scale_blocks(N);
   cudaError_t e = fa::launch_quant_e4m3(static_cast<const __nv_bfloat16*>(q),
-                                        q8, sq, BH, N, d, nsb,
+                                        q8, sq, BH, N, d, nsb, kFp8RowBytes,
                                         ctx->sm_count * 8, st);
   if (e == cudaSuccess)
     e = fa::launch_quant_e4m3(static_cast<const __nv_bfloat16*>(k), k8, sk, BH,
-                              N, d, nsb, ctx->sm_count * 8, st);
+                              N, d, nsb, kFp8RowBytes, ctx->sm_count * 8, st);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -616,7 +618,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.timeout_ns = kernel_timeout();
   a.hook = g_hook_on.load() ? 1 : 0;
   fwd_sched_slot(ctx, a);
-  e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, causal != 0, ctx->sm_count, st);
+  e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, d, causal != 0, ctx->sm_count, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -142,7 +142,7 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc,
   }
 }
 
-// FP8 path: S_t = Q8_t K8^T with E4M3 operands, K = d = 128 in four steps
+// FP8 path: S_t = Q8_t K8^T with E4M3 operands, K = 128 in four steps
 // of 32 elements (32 bytes) along one 128-byte row; scales are applied by
 // the softmax.
 __device__ __forceinline__ void issue_qk_fp8(uint32_t s_tmem, uint64_t q_desc,
@@ -428,10 +428,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = FwdLayout<D>;
   constexpr int S = L::kStages;
-  // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 (one
-  // byte per element, d = 128: a single box) on the FP8 path.
-  static_assert(!FP8 || D == 128, "the FP8 path needs d = 128");
-  constexpr uint32_t kQKBytes = FP8 ? kTile * D : L::kTileBytes;
+  // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 on
+  // the FP8 path: one byte per element in rows of 128 bytes (at d = 64 the
+  // upper half of each row is zero, so the product is that of d = 128), a
+  // single box.
+  static_assert(!FP8 || D == 128 || D == 64, "the FP8 path needs d = 64 or 128");
+  constexpr uint32_t kQKBytes = FP8 ? kTile * 128 : L::kTileBytes;
   constexpr int kQKBoxes = FP8 ? 1 : L::kSub;
   static_assert(sizeof(FwdBars<S>) <= kFwdBarBytes, "barrier block");
   extern __shared__ uint8_t smem_raw[];
@@ -992,11 +994,13 @@ cudaError_t launch_fwd_w(const CUtensorMap& tq, const CUtensorMap& tk,
 // block, scale = amax / 448 (1 for an all-zero block), codes = round to
 // nearest even of x / scale with saturation.  Both divisions are IEEE
 // round-to-nearest, so the codes are those of the same float32 arithmetic
-// anywhere.  Lane l holds columns [l*D/32, (l+1)*D/32) of every row.
+// anywhere.  Lane l holds columns [l*D/32, (l+1)*D/32) of every row.  Code
+// rows are `pitch` bytes apart (pitch >= D); bytes D .. pitch - 1 of a row
+// are written as zero (the FP8 forward pads d = 64 rows to 128 bytes).
 template <int D>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(
     const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
-    float* __restrict__ scales, int BH, int N, int n_sblk) {
+    float* __restrict__ scales, int BH, int N, int n_sblk, int pitch) {
   constexpr int kPer = D / 32;
   const int lane = threadIdx.x & 31;
   const long long n_blk = (long long)BH * n_sblk;
@@ -1011,6 +1015,7 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(
       continue;
     }
     const size_t base = ((size_t)bh * N + r0) * D + lane * kPer;
+    const size_t cbase = ((size_t)bh * N + r0) * pitch + lane * kPer;
     float v[16][kPer];
     float amax = 0.f;
 #pragma unroll
@@ -1038,7 +1043,9 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       if (r >= rows) break;
-      uint8_t* dst = codes + base + (size_t)r * D;
+      uint8_t* dst = codes + cbase + (size_t)r * pitch;
+      for (int c = D; c < pitch; c += 32 * kPer)  // zero padding of the row
+        for (int e = 0; e < kPer; ++e) dst[c + e] = 0;
       if constexpr (kPer == 4) {
         const uint32_t lo = pack_e4m3(__fdiv_rn(v[r][0], sc), __fdiv_rn(v[r][1], sc));
         const uint32_t hi = pack_e4m3(__fdiv_rn(v[r][2], sc), __fdiv_rn(v[r][3], sc));
@@ -1056,17 +1063,22 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(
 
 cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
                               float* scales, int BH, int N, int d, int n_sblk,
-                              int grid_blocks, cudaStream_t stream) {
+                              int pitch, int grid_blocks, cudaStream_t stream) {
   if (d == 128)
-    quant_e4m3_kernel<128><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N, n_sblk);
+    quant_e4m3_kernel<128><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N,
+                                                           n_sblk, pitch);
   else
-    quant_e4m3_kernel<64><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N, n_sblk);
+    quant_e4m3_kernel<64><<<grid_blocks, 256, 0, stream>>>(x, codes, scales, BH, N,
+                                                          n_sblk, pitch);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdArgs& a, int BH,
+                           const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
                            bool causal, int grid_blocks, cudaStream_t stream) {
+  if (d == 64)
+    return causal ? launch_fwd_t<64, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+                  : launch_fwd_t<64, false, false, true>(tq, tk, tv, a, BH, grid_blocks, stream);
   return causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
                 : launch_fwd_t<128, false, false, true>(tq, tk, tv, a, BH, grid_blocks, stream);
 }

@@ -81,16 +81,18 @@ struct BwdArgs {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
                        bool causal, int grid_blocks, cudaStream_t stream);
-// FP8 forward: tq, tk are E4M3 tensor maps (one byte per element), tv the
-// bf16 V map; d = 128 only.
+// FP8 forward: tq, tk are E4M3 tensor maps (one byte per element, rows of
+// 128 bytes: at d = 64 the upper half of each row is zero), tv the bf16 V
+// map; d = 64 or 128.
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdArgs& a, int BH,
+                           const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
                            bool causal, int grid_blocks, cudaStream_t stream);
 // E4M3 codes and per-16-row-block scales of a bf16 [BH, N, d] tensor
 // (d = 64 or 128); scales has BH * n_sblk entries, 1 for blocks past N.
+// Code rows are `pitch` bytes apart (>= d), bytes d .. pitch - 1 zero.
 cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
                               float* scales, int BH, int N, int d, int n_sblk,
-                              int grid_blocks, cudaStream_t stream);
+                              int pitch, int grid_blocks, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, int grid_blocks,
                            cudaStream_t stream);
 // Persistent: min(work items, grid_blocks) blocks, one per SM.
