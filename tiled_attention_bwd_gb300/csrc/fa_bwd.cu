@@ -23,10 +23,13 @@
 //   post  dQ = scale * accumulator, rounded to bf16.
 //
 // Warps of the main kernel:
-//   0-3  thread = key row: P^T = exp2(S^T c + LSE2), then dS^T = P^T (dP^T - D)
+//   0-3  thread = key row: P^T = exp2(S^T c + LSE2), then dS^T = P^T (dP^T - D);
+//        at the end of an item the dK_j read-out, staged in the dS tile and
+//        sent by TMA store
 //   4-7  thread = query row: drain dQ_i from TMEM, stage it box by box
-//        through two 16 KB buffers and add it into the fp32 accumulator with
-//        TMA reduce-add
+//        through two 4 KB boxes per warp and add it into the fp32
+//        accumulator with TMA reduce-add; at the end of an item the dV_j
+//        read-out, staged in the same boxes and sent by TMA store
 //   8    TMA producer,  9  MMA issuer (one thread) and TMEM owner.
 // TMEM columns (512 allocated): S^T/P^T [0,128)  dP^T, then dS^T (bf16
 // pairs in [128,192)), then dQ [128,256)  dK [256, 256+d)  dV [256+d, 256+2d).

@@ -8,8 +8,10 @@
 // Design Spec", Item 3, sections "TMA" and "Warp Specialization").
 //
 // Persistent blocks (one per SM) take work items of two 128-row Q tiles of
-// one (batch, head) and stream the 128-row K/V tiles past them:
-//   warp 8      TMA producer: Q0, Q1 once per item; K_j, V_j through a ring.
+// one (batch, head), or of one tile when a problem has fewer pairs than
+// SMs, and stream the 128-row K/V tiles past them:
+//   warp 8      TMA producer: Q0, Q1 once per item (three rotating
+//               buffers, q_buf); K_j, V_j through a ring.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //               O_t += P_t V_j with P_t read straight from TMEM.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1; thread = row.
