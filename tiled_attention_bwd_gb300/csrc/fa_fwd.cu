@@ -69,13 +69,17 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 // smem) ran at full rate.  Issued back to back with no waits, every form runs
 // at full rate, so the smem x smem cost is latency on a dependent path.
 // Hence 128-key tiles, P kept in TMEM, and two Q tiles whose MMAs interleave.
-template <int D>
+// QBUFS: 3 Q buffers for the rotation of q_buf, 2 for the banded (WINDOW)
+// kernels, which keep tile t in buffer t.  Those include the kernels with
+// per-sequence lengths, whose balanced item table takes the shared memory
+// left after the tiles: about 32 KB with two buffers, 1.8 KB with three.
+template <int D, int QBUFS = 3>
 struct FwdLayout {
   static constexpr int kSub = D / 64;             // 64-column sub-tiles
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 128) ? 4 : 6;
   static constexpr int kQOff = 0;
-  static constexpr int kQBufs = 3;
+  static constexpr int kQBufs = QBUFS;
   static constexpr int kKVOff = kQBufs * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
@@ -122,8 +126,8 @@ enum : uint32_t {
 // issued while the current item's last key tiles run, instead of waiting
 // for its tile 1 to let go of its buffer: buffers (t0, t1, spare) run
 // (0, 1, 2), (2, 0, 1), (1, 2, 0), ...  The banded (WINDOW) kernels keep
-// tile t in buffer t: the rotation's state in their 96-register control
-// warps cost them 3-4%.
+// two buffers, tile t in buffer t (see FwdLayout): the rotation cost them
+// 3-4%.
 __device__ __forceinline__ int q_buf(uint32_t n, int t) {
   const int r = (int)(n % 3u);
   return (t == 0 ? 3 - r : 4 - r) % 3;
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, WINDOW ? 2 : 3>;
   constexpr int S = L::kStages;
   // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 on
   // the FP8 path: one byte per element in rows of 128 bytes (at d = 64 the
@@ -919,7 +923,7 @@ template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN = false,
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdArgs& a, int BH,
                          int grid_blocks, cudaStream_t stream) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, WINDOW ? 2 : 3>;
   static_assert(!VARLEN || (WINDOW && !FP8), "lengths run windowed, bf16");
   static_assert(!DYN || !WINDOW, "banded calls use the alternating rounds");
   // The failure-path test hook has its own instantiation, for d = 128 bf16
