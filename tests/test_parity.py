@@ -124,6 +124,29 @@ def test_forward_is_deterministic():
     assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_output_only_16_byte_aligned(d):
+    # O rows leave in 32-byte stores when O is 32-byte aligned, else in
+    # 16-byte ones (the boundary asks for 16): both give the same bits.
+    dev = torch.device("cuda:0")
+    B, H, N, causal = 1, 3, 333, True
+    scale = default_scale(d)
+    inp = make_inputs(B, H, N, d, seed=37)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    n = q.numel()
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dev)
+    o16 = buf[8:].view(q.shape)                   # 16 bytes past a 256-byte base
+    assert o16.data_ptr() % 16 == 0 and o16.data_ptr() % 32 != 0
+    o16.fill_(float("nan"))
+    o16, lse16 = fa_fwd(q, k, v, causal, scale, out=o16)
+    o32, lse32 = fa_fwd(q, k, v, causal, scale)
+    assert o32.data_ptr() % 32 == 0
+    assert fa_check_device_status(dev) == 0
+    assert torch.equal(o16, o32) and torch.equal(lse16, lse32)
+    o_ref, lse_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], causal, scale)
+    check_forward(o16, lse16, o_ref, lse_ref, "16-byte aligned O")
+
+
 # ----------------------------------------------------------- invariants
 @pytest.mark.parametrize("causal", [False, True])
 def test_gpu_invariants(causal):

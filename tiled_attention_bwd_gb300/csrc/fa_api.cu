@@ -349,6 +349,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   if ((s = make_tile_map(&tv, v, BHkv, N, d)) != FA_OK) return s;
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.o_wide = aligned(o, 32) ? 1 : 0;
   a.lse = lse;
   a.BH = BH;
   a.N = N;
@@ -602,6 +603,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   if (e != cudaSuccess) return FA_ERR_CUDA;
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.o_wide = aligned(o, 32) ? 1 : 0;
   a.lse = lse;
   a.BH = BH;
   a.N = N;

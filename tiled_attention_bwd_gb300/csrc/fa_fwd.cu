@@ -887,11 +887,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
                             __uint_as_float(o[2 * e + 1]) * inv_l);
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+          if (a.o_wide) {  // whole 32-byte sectors (rows are d * 2 bytes apart)
+            st_global_v8(orow + ch * 32, pk);
+            st_global_v8(orow + ch * 32 + 16, pk + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                 pk[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                   pk[4 * v4 + 3]);
+          }
         }
       }
       if (valid) a.lse[(size_t)itm.bh * a.N + qrow] = (m_ref + lg2(l)) * kLn2;

@@ -12,6 +12,7 @@ struct DevState;
 
 struct FwdArgs {
   __nv_bfloat16* o;     // [BH, N, d]
+  int o_wide;           // 1: o is 32-byte aligned (rows leave in 32-byte stores)
   float* lse;           // [BH, N]
   int BH;               // batch x query heads
   int N;

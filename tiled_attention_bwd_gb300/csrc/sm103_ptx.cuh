@@ -122,6 +122,15 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reads operands through it).
+// One 32-byte global store (a whole sector) from eight registers; the
+// address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),
+                  "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
