@@ -147,6 +147,23 @@ def test_output_only_16_byte_aligned(d):
     check_forward(o16, lse16, o_ref, lse_ref, "16-byte aligned O")
 
 
+@pytest.mark.parametrize("H,N,d", [(120, 1700, 128), (100, 4000, 64)])
+def test_dynamic_schedule_ragged(H, N, d):
+    # K and V of all heads above 96 MB (4 N d bytes per head) select the
+    # head-grouped dynamic schedule, whose kernels store O through shared
+    # memory by TMA; a ragged N makes the stores of the last tile clip.
+    assert H * 4 * N * d > 96 << 20 and N % 128 != 0
+    causal, scale = True, default_scale(d)
+    inp = make_inputs(1, H, N, d, seed=53 + d)
+    got = run_gpu(inp, causal, scale, backward=False)
+    heads = sample_heads(H, 6, seed=N)
+    assert heads[0] == 0 and heads[-1] == H - 1
+    sub = {n: heads_of(inp[n], heads) for n in ("q", "k", "v")}
+    o_ref, lse_ref = oracle.fwd(sub["q"], sub["k"], sub["v"], causal, scale)
+    check_forward(heads_of(got["o"], heads), heads_of(got["lse"], heads),
+                  o_ref, lse_ref, "dynamic schedule H=%d N=%d d=%d" % (H, N, d))
+
+
 # ----------------------------------------------------------- invariants
 @pytest.mark.parametrize("causal", [False, True])
 def test_gpu_invariants(causal):

@@ -347,6 +347,8 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   if ((s = make_tile_map(&tq, q, BH, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tk, k, BHkv, N, d)) != FA_OK) return s;
   if ((s = make_tile_map(&tv, v, BHkv, N, d)) != FA_OK) return s;
+  CUtensorMap to;  // O, stored by TMA in 32-row boxes
+  if ((s = make_tile_map(&to, o, BH, N, d, 32)) != FA_OK) return s;
   fa::FwdArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
   a.o_wide = aligned(o, 32) ? 1 : 0;
@@ -366,7 +368,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o,
   a.timeout_ns = kernel_timeout();
   a.hook = g_hook_on.load() ? 1 : 0;
   fwd_sched_slot(ctx, a);
-  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, BH, d, causal != 0,
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, to, a, BH, d, causal != 0,
                                  ctx->sm_count, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -592,6 +594,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   if ((s = make_fp8_map(&tq, q8, BH, N, kFp8RowBytes)) != FA_OK) return s;
   if ((s = make_fp8_map(&tk, k8, BH, N, kFp8RowBytes)) != FA_OK) return s;
   if ((s = make_tile_map(&tv, v, BH, N, d)) != FA_OK) return s;
+  CUtensorMap to;  // O (the FP8 kernels store it from registers)
+  if ((s = make_tile_map(&to, o, BH, N, d, 32)) != FA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int nsb = scale_blocks(N);
   cudaError_t e = fa::launch_quant_e4m3(static_cast<const __nv_bfloat16*>(q),
@@ -620,7 +624,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.timeout_ns = kernel_timeout();
   a.hook = g_hook_on.load() ? 1 : 0;
   fwd_sched_slot(ctx, a);
-  e = fa::launch_fwd_fp8(tq, tk, tv, a, BH, d, causal != 0, ctx->sm_count, st);
+  e = fa::launch_fwd_fp8(tq, tk, tv, to, a, BH, d, causal != 0, ctx->sm_count, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

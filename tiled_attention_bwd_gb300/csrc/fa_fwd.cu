@@ -18,6 +18,9 @@
 //               exp2 with the scale folded in, lazy rescaling of O (only when
 //               the row max grows by more than 2^8), P written back to TMEM
 //               as bf16 over the S columns it came from.
+// At the end of an item each softmax thread writes its row of O: by TMA
+// store through a per-warp box in shared memory in the dynamic-schedule
+// kernels, in 32-byte (else 16-byte) stores from registers in the others.
 // While one softmax group works on its tile the tensor core runs the other
 // tile's MMAs (ping-pong).  Causal blocks stop at the diagonal tile; only the
 // diagonal (and a ragged last tile) is masked.
@@ -73,15 +76,22 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 // kernels, which keep tile t in buffer t.  Those include the kernels with
 // per-sequence lengths, whose balanced item table takes the shared memory
 // left after the tiles: about 32 KB with two buffers, 1.8 KB with three.
-template <int D, int QBUFS = 3>
+// OSTG: O leaves through shared memory by TMA store, one [32 rows][64
+// columns] bf16 box (4 KB, 128-byte swizzle) per softmax warp; at d = 128
+// the K/V ring gives up a stage for it (measured no slower with the dynamic
+// schedule, whose K/V come from DRAM; the static one lost 6.5% at
+// 4x32x1024, so it keeps four stages and stores O from registers).
+template <int D, int QBUFS = 3, bool OSTG = false>
 struct FwdLayout {
   static constexpr int kSub = D / 64;             // 64-column sub-tiles
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 128) ? 4 : 6;
+  static constexpr int kStages = (D == 128) ? (OSTG ? 3 : 4) : 6;
   static constexpr int kQOff = 0;
   static constexpr int kQBufs = QBUFS;
   static constexpr int kKVOff = kQBufs * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kOStgOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kOStgBoxBytes = 32 * 128;
+  static constexpr int kBarOff = kOStgOff + (OSTG ? 8 * kOStgBoxBytes : 0);
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
 };
 // Bytes reserved for the barriers; the item table of the VARLEN kernels
@@ -431,8 +441,11 @@ template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN, bool DYN,
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using L = FwdLayout<D, WINDOW ? 2 : 3>;
+               const __grid_constant__ CUtensorMap tm_v,
+               const __grid_constant__ CUtensorMap tm_o, const FwdArgs a) {
+  // O through shared memory and TMA store: the dynamic-schedule bf16 kernels.
+  constexpr bool OSTG = DYN && !FP8;
+  using L = FwdLayout<D, WINDOW ? 2 : 3, OSTG>;
   constexpr int S = L::kStages;
   // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 on
   // the FP8 path: one byte per element in rows of 128 bytes (at d = 64 the
@@ -502,6 +515,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      if constexpr (OSTG) prefetch_tmap(&tm_o);
       int last_par[S];
 #pragma unroll
       for (int s = 0; s < S; ++s) last_par[s] = -1;
@@ -707,6 +721,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tl + 256 + t * D;
     const float c = a.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;
+    bool ostg_pending = false;  // this warp's O box is being stored
     bool ok = run;
     for (int ti = 0; ok; ++ti) {
       int w;
@@ -874,28 +889,67 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // The length is read again rather than kept live through the loop.
       const bool valid =
           qrow < (VARLEN ? seq_len_of(a.seq_lens, itm.bh / a.H, a.N) : a.N);
-      __nv_bfloat16* orow = a.o + ((size_t)itm.bh * a.N + (valid ? qrow : 0)) * D;
+      if constexpr (OSTG) {
+        // 64 columns at a time: the row goes into this warp's box (row =
+        // lane, 16-byte pieces in the 128-byte swizzle) and the box leaves
+        // by TMA store, which clips rows past N.  The box is rewritten only
+        // after the previous store has read it.
+        uint8_t* const box = smem + L::kOStgOff + warp * L::kOStgBoxBytes;
+        uint8_t* const brow = box + lane * 128;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(tO + ch * 32, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-        uint32_t pk[16];
+        for (int hb = 0; hb < D / 64; ++hb) {
+          if (ostg_pending) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
-                            __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (valid) {
-          if (a.o_wide) {  // whole 32-byte sectors (rows are d * 2 bytes apart)
-            st_global_v8(orow + ch * 32, pk);
-            st_global_v8(orow + ch * 32 + 16, pk + 8);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + hb * 64 + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
+                                __uint_as_float(o[2 * e + 1]) * inv_l);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                   pk[4 * v4 + 3]);
+              *reinterpret_cast<uint4*>(brow + (((c * 4 + v4) ^ (lane & 7)) * 16)) =
+                  make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tm_o, box, hb * 64, q0 + quarter * 32, itm.bh);
+            bulk_commit_group();
+          }
+          ostg_pending = true;
+        }
+      } else {
+        __nv_bfloat16* orow = a.o + ((size_t)itm.bh * a.N + (valid ? qrow : 0)) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + ch * 32, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
+                              __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (valid) {
+            if (a.o_wide) {  // whole 32-byte sectors (rows are d * 2 bytes apart)
+              st_global_v8(orow + ch * 32, pk);
+              st_global_v8(orow + ch * 32 + 16, pk + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                     pk[4 * v4 + 3]);
+            }
           }
         }
       }
@@ -904,6 +958,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // this warp group's next p_full arrival, so O_t is read out first.
       tc_fence_before();
     }
+    // O stores complete (and done reading shared memory) before exit.
+    if (OSTG && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -926,9 +982,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int D, bool CAUSAL, bool WINDOW, bool FP8, bool VARLEN = false,
           bool DYN = false, bool HOOK = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const FwdArgs& a, int BH,
-                         int grid_blocks, cudaStream_t stream) {
-  using L = FwdLayout<D, WINDOW ? 2 : 3>;
+                         const CUtensorMap& tv, const CUtensorMap& to,
+                         const FwdArgs& a, int BH, int grid_blocks,
+                         cudaStream_t stream) {
+  using L = FwdLayout<D, WINDOW ? 2 : 3, DYN && !FP8>;
   static_assert(!VARLEN || (WINDOW && !FP8), "lengths run windowed, bf16");
   static_assert(!DYN || !WINDOW, "banded calls use the alternating rounds");
   // The failure-path test hook has its own instantiation, for d = 128 bf16
@@ -936,13 +993,13 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   if constexpr (D == 128 && !WINDOW && !FP8 && !VARLEN && !DYN && !HOOK) {
     if (a.hook)
       return launch_fwd_t<D, CAUSAL, WINDOW, FP8, VARLEN, false, true>(
-          tq, tk, tv, a, BH, grid_blocks, stream);
+          tq, tk, tv, to, a, BH, grid_blocks, stream);
   }
   // The dynamic schedule exists only without a window: the host asks for it
   // (a.dynamic) only there.
   if constexpr (!WINDOW && !DYN && !HOOK) {
     if (a.dynamic)
-      return launch_fwd_t<D, CAUSAL, WINDOW, FP8, VARLEN, true>(tq, tk, tv, a, BH,
+      return launch_fwd_t<D, CAUSAL, WINDOW, FP8, VARLEN, true>(tq, tk, tv, to, a, BH,
                                                               grid_blocks, stream);
   }
   auto kern = fwd_kernel<D, CAUSAL, WINDOW, FP8, VARLEN, DYN, HOOK>;
@@ -984,21 +1041,22 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   if (e != cudaSuccess) return e;
   const int n_items = BH * n_pairs;
   const int blocks = n_items < grid_blocks ? n_items : grid_blocks;
-  kern<<<blocks, kFwdThreads, smem_bytes, stream>>>(tq, tk, tv, args);
+  kern<<<blocks, kFwdThreads, smem_bytes, stream>>>(tq, tk, tv, to, args);
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_w(const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const FwdArgs& a, int BH,
-                         int grid_blocks, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& to,
+                         const FwdArgs& a, int BH, int grid_blocks,
+                         cudaStream_t stream) {
   if (a.seq_lens)  // the host passes a window (N - 1 at widest) with lengths
     return a.window >= 0
-               ? launch_fwd_t<D, CAUSAL, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
+               ? launch_fwd_t<D, CAUSAL, true, false, true>(tq, tk, tv, to, a, BH, grid_blocks, stream)
                : cudaErrorInvalidValue;
   return a.window >= 0
-             ? launch_fwd_t<D, CAUSAL, true, false>(tq, tk, tv, a, BH, grid_blocks, stream)
-             : launch_fwd_t<D, CAUSAL, false, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+             ? launch_fwd_t<D, CAUSAL, true, false>(tq, tk, tv, to, a, BH, grid_blocks, stream)
+             : launch_fwd_t<D, CAUSAL, false, false>(tq, tk, tv, to, a, BH, grid_blocks, stream);
 }
 
 // E4M3 quantisation, one warp per 16-row block of one head: amax of the
@@ -1085,23 +1143,25 @@ cudaError_t launch_quant_e4m3(const __nv_bfloat16* x, uint8_t* codes,
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                           bool causal, int grid_blocks, cudaStream_t stream) {
+                           const CUtensorMap& tv, const CUtensorMap& to,
+                           const FwdArgs& a, int BH, int d, bool causal,
+                           int grid_blocks, cudaStream_t stream) {
   if (d == 64)
-    return causal ? launch_fwd_t<64, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                  : launch_fwd_t<64, false, false, true>(tq, tk, tv, a, BH, grid_blocks, stream);
-  return causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                : launch_fwd_t<128, false, false, true>(tq, tk, tv, a, BH, grid_blocks, stream);
+    return causal ? launch_fwd_t<64, true, false, true>(tq, tk, tv, to, a, BH, grid_blocks, stream)
+                  : launch_fwd_t<64, false, false, true>(tq, tk, tv, to, a, BH, grid_blocks, stream);
+  return causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, to, a, BH, grid_blocks, stream)
+                : launch_fwd_t<128, false, false, true>(tq, tk, tv, to, a, BH, grid_blocks, stream);
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                       bool causal, int grid_blocks, cudaStream_t stream) {
+                       const CUtensorMap& tv, const CUtensorMap& to,
+                       const FwdArgs& a, int BH, int d, bool causal,
+                       int grid_blocks, cudaStream_t stream) {
   if (d == 128)
-    return causal ? launch_fwd_w<128, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                  : launch_fwd_w<128, false>(tq, tk, tv, a, BH, grid_blocks, stream);
-  return causal ? launch_fwd_w<64, true>(tq, tk, tv, a, BH, grid_blocks, stream)
-                : launch_fwd_w<64, false>(tq, tk, tv, a, BH, grid_blocks, stream);
+    return causal ? launch_fwd_w<128, true>(tq, tk, tv, to, a, BH, grid_blocks, stream)
+                  : launch_fwd_w<128, false>(tq, tk, tv, to, a, BH, grid_blocks, stream);
+  return causal ? launch_fwd_w<64, true>(tq, tk, tv, to, a, BH, grid_blocks, stream)
+                : launch_fwd_w<64, false>(tq, tk, tv, to, a, BH, grid_blocks, stream);
 }
 
 cudaError_t set_expire_site_fwd(uint32_t site) {

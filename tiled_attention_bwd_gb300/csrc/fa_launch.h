@@ -78,16 +78,20 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
-// Each returns the launch error (cudaSuccess on success).
+// Each returns the launch error (cudaSuccess on success).  `to` maps O
+// ([BH, N, d] bf16, boxes of 32 rows x 64 columns, 128-byte swizzle) for the
+// kernels that store O by TMA.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                       bool causal, int grid_blocks, cudaStream_t stream);
+                       const CUtensorMap& tv, const CUtensorMap& to,
+                       const FwdArgs& a, int BH, int d, bool causal,
+                       int grid_blocks, cudaStream_t stream);
 // FP8 forward: tq, tk are E4M3 tensor maps (one byte per element, rows of
 // 128 bytes: at d = 64 the upper half of each row is zero), tv the bf16 V
 // map; d = 64 or 128.
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdArgs& a, int BH, int d,
-                           bool causal, int grid_blocks, cudaStream_t stream);
+                           const CUtensorMap& tv, const CUtensorMap& to,
+                           const FwdArgs& a, int BH, int d, bool causal,
+                           int grid_blocks, cudaStream_t stream);
 // E4M3 codes and per-16-row-block scales of a bf16 [BH, N, d] tensor
 // (d = 64 or 128); scales has BH * n_sblk entries, 1 for blocks past N.
 // Code rows are `pitch` bytes apart (>= d), bytes d .. pitch - 1 zero.
