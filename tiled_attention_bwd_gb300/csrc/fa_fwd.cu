@@ -19,8 +19,9 @@
 //               the row max grows by more than 2^8), P written back to TMEM
 //               as bf16 over the S columns it came from.
 // At the end of an item each softmax thread writes its row of O: by TMA
-// store through a per-warp box in shared memory in the dynamic-schedule
-// kernels, in 32-byte (else 16-byte) stores from registers in the others.
+// store through a per-warp box in shared memory in the dynamic-schedule and
+// windowed kernels, in 32-byte (else 16-byte) stores from registers in the
+// others.
 // While one softmax group works on its tile the tensor core runs the other
 // tile's MMAs (ping-pong).  Causal blocks stop at the diagonal tile; only the
 // diagonal (and a ragged last tile) is masked.
@@ -77,15 +78,16 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: factor 256
 // per-sequence lengths, whose balanced item table takes the shared memory
 // left after the tiles: about 32 KB with two buffers, 1.8 KB with three.
 // OSTG: O leaves through shared memory by TMA store, one [32 rows][64
-// columns] bf16 box (4 KB, 128-byte swizzle) per softmax warp; at d = 128
-// the K/V ring gives up a stage for it (measured no slower with the dynamic
-// schedule, whose K/V come from DRAM; the static one lost 6.5% at
-// 4x32x1024, so it keeps four stages and stores O from registers).
+// columns] bf16 box (4 KB, 128-byte swizzle) per softmax warp.  With three
+// Q buffers at d = 128 the K/V ring gives up a stage for it (measured no
+// slower with the dynamic schedule, whose K/V come from DRAM; the static
+// one lost 6.5% at 4x32x1024, so it keeps four stages and stores O from
+// registers); the banded kernels' two Q buffers leave room for it.
 template <int D, int QBUFS = 3, bool OSTG = false>
 struct FwdLayout {
   static constexpr int kSub = D / 64;             // 64-column sub-tiles
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 128) ? (OSTG ? 3 : 4) : 6;
+  static constexpr int kStages = (D == 128) ? ((OSTG && QBUFS == 3) ? 3 : 4) : 6;
   static constexpr int kQOff = 0;
   static constexpr int kQBufs = QBUFS;
   static constexpr int kKVOff = kQBufs * kTileBytes;
@@ -97,6 +99,12 @@ struct FwdLayout {
 // Bytes reserved for the barriers; the item table of the VARLEN kernels
 // follows them.
 constexpr int kFwdBarBytes = 256;
+
+// Kernels whose O leaves by TMA store: bf16, with the dynamic schedule or a
+// window (not per-sequence lengths, whose padding rows stay untouched and
+// whose item table takes the shared memory).
+template <bool WINDOW, bool FP8, bool VARLEN, bool DYN>
+constexpr bool fwd_ostg() { return !FP8 && !VARLEN && (DYN || WINDOW); }
 
 template <int STAGES>
 struct FwdBars {
@@ -443,8 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_o, const FwdArgs a) {
-  // O through shared memory and TMA store: the dynamic-schedule bf16 kernels.
-  constexpr bool OSTG = DYN && !FP8;
+  constexpr bool OSTG = fwd_ostg<WINDOW, FP8, VARLEN, DYN>();
   using L = FwdLayout<D, WINDOW ? 2 : 3, OSTG>;
   constexpr int S = L::kStages;
   // Bytes and 128-byte-wide TMA boxes of one Q or K tile: bf16, or E4M3 on
@@ -985,7 +992,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& to,
                          const FwdArgs& a, int BH, int grid_blocks,
                          cudaStream_t stream) {
-  using L = FwdLayout<D, WINDOW ? 2 : 3, DYN && !FP8>;
+  using L = FwdLayout<D, WINDOW ? 2 : 3, fwd_ostg<WINDOW, FP8, VARLEN, DYN>()>;
   static_assert(!VARLEN || (WINDOW && !FP8), "lengths run windowed, bf16");
   static_assert(!DYN || !WINDOW, "banded calls use the alternating rounds");
   // The failure-path test hook has its own instantiation, for d = 128 bf16
