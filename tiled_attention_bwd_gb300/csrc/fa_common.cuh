@@ -58,6 +58,10 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t where) {
 // Wait for the phase of `bar` with the given parity.  Returns false (and
 // never blocks longer than the time limit) if the wait expired here or the
 // block / grid is already stopping.
+// Longest a polling thread sleeps in one try_wait before it looks at the
+// abort flags and the clock again (it wakes as soon as the phase completes).
+constexpr uint32_t kPollHintNs = 100000;
+
 template <bool kHook>
 __device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
                                               const WaitCtl& c, uint32_t where) {
@@ -67,7 +71,7 @@ __device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
   while (true) {
 #pragma unroll 1
     for (int i = hook ? 64 : 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_hint(bar, parity, kPollHintNs)) return true;
     if (ld_volatile_u32(c.cta_abort)) return false;
     if (*reinterpret_cast<volatile unsigned int*>(&c.st->abort)) {
       *reinterpret_cast<volatile uint32_t*>(c.cta_abort) = 1u;

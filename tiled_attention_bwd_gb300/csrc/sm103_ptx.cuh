@@ -37,6 +37,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
                "r"(bytes)
                : "memory");
 }
+// As mbar_try_wait, but the thread may stay suspended in the instruction up
+// to `hint_ns` nanoseconds while the phase is incomplete (it resumes when
+// the phase completes), so a waiting warp polls shared memory less often.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
