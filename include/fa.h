@@ -22,8 +22,9 @@
  *  - Tensors q, k, v, o, dout, dq, dk, dv are contiguous row-major bfloat16
  *    arrays of shape [B, H, N, d] in device memory (element (b,h,i,t) at
  *    ((b*H + h)*N + i)*d + t).  Their base addresses must be 16-byte aligned;
- *    a forward whose o is also 32-byte aligned writes it in whole 32-byte
- *    sectors (faster, same values).
+ *    where the forward stores O from registers (problems whose K and V fit
+ *    in L2, without a window), a 32-byte-aligned o is written in whole
+ *    32-byte sectors (faster, same values).
  *  - lse is a contiguous float32 array [B, H, N] in device memory holding the
  *    natural-log log-sum-exp of each row's scaled scores:
  *    lse[b,h,i] = ln sum_j exp(scale * q_i . k_j) over the visible keys j.

@@ -55,13 +55,13 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t where) {
   *reinterpret_cast<volatile uint32_t*>(c.cta_abort) = 1u;
 }
 
-// Wait for the phase of `bar` with the given parity.  Returns false (and
-// never blocks longer than the time limit) if the wait expired here or the
-// block / grid is already stopping.
 // Longest a polling thread sleeps in one try_wait before it looks at the
 // abort flags and the clock again (it wakes as soon as the phase completes).
 constexpr uint32_t kPollHintNs = 100000;
 
+// Wait for the phase of `bar` with the given parity.  Returns false (and
+// never blocks longer than the time limit) if the wait expired here or the
+// block / grid is already stopping.
 template <bool kHook>
 __device__ __forceinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
                                               const WaitCtl& c, uint32_t where) {
